@@ -1,0 +1,19 @@
+"""Sharded ring attention for one GB300 (sm_103a).
+
+Python surface of the C-ABI library (include/st_attn.h); the functions keep
+the C names.  See ``_lib`` for the marshalling and ``workloads`` for the
+seeded synthetic inputs.
+"""
+from ._lib import (  # noqa: F401
+    Layout,
+    StAttnError,
+    load,
+    st_attn_bwd,
+    st_attn_fwd,
+    st_attn_fwd_partials,
+    st_attn_merge,
+    st_attn_workspace_size,
+    st_permute,
+    ST_DTYPE_BF16,
+    ST_DTYPE_F32,
+)

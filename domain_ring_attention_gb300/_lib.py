@@ -1,0 +1,240 @@
+"""ctypes binding of the C-ABI in include/st_attn.h.
+
+Argument marshalling only: every step of the computation runs inside the
+CUDA library.  PyTorch provides device memory and the current stream.  If the
+library has not been built, loading fails with an error; there is no other
+implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libst_attn.so")
+
+ST_DTYPE_F32 = 0
+ST_DTYPE_BF16 = 1
+ST_MAX_SHARDS = 32
+
+ERRORS = {
+    0: "ST_OK", -1: "ST_ERR_NULL", -2: "ST_ERR_INVALID_LAYOUT", -3: "ST_ERR_UNSUPPORTED",
+    -4: "ST_ERR_MISALIGNED", -5: "ST_ERR_WORKSPACE", -6: "ST_ERR_CUDA",
+    -7: "ST_ERR_DEVICE_TIMEOUT", -8: "ST_ERR_INVALID_ARG",
+}
+
+# C prototypes: (name, restype, argtypes)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+PROTOTYPES = [
+    ("st_layout_create", _I, [ctypes.POINTER(_I64), _I, _I, ctypes.POINTER(_P)]),
+    ("st_layout_destroy", _I, [_P]),
+    ("st_layout_query", _I, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64),
+                             ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    ("st_attn_workspace_size", _I, [_P, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
+    ("st_attn_fwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    ("st_attn_fwd_partials", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P]),
+    ("st_attn_merge", _I, [_I, _I, _I, _I64, _I, _P, _P, _P, _P, _I, _P]),
+    ("st_attn_bwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
+                         _SZ, _P]),
+    ("st_permute", _I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    ("st_error_string", ctypes.c_char_p, [_I]),
+    ("st_last_cuda_error", _I, []),
+]
+
+_lib = None
+
+
+class StAttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = "%s failed: %s (%d)" % (where, ERRORS.get(code, "?"), code)
+        if _lib is not None:
+            msg += ": " + _lib.st_error_string(code).decode()
+            if code == -6:
+                msg += " [cudaError %d]" % _lib.st_last_cuda_error()
+        super().__init__(msg)
+
+
+def load():
+    """Load the shared library (once).  Raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libst_attn.so is not built (run __graft_entry__.build() "
+                               "or python -m domain_ring_attention_gb300.build)")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, res, args in PROTOTYPES:
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise StAttnError(rc, where)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(dt):
+    if dt == torch.float32:
+        return ST_DTYPE_F32
+    if dt == torch.bfloat16:
+        return ST_DTYPE_BF16
+    raise TypeError("only float32 and bfloat16 tensors are supported, got %s" % dt)
+
+
+class Layout:
+    """Owner of an ``st_layout_t`` built from sharding shapes."""
+
+    def __init__(self, shard_lens, zigzag: bool = False):
+        lib = load()
+        lens = [int(x) for x in shard_lens]
+        arr = (_I64 * max(1, len(lens)))(*lens)
+        h = ctypes.c_void_p()
+        _check(lib.st_layout_create(arr, len(lens), int(bool(zigzag)), ctypes.byref(h)),
+               "st_layout_create")
+        self._h = h
+        self.lens = lens
+        self.zigzag = bool(zigzag)
+        S = _I64()
+        _check(lib.st_layout_query(h, ctypes.byref(S), None, None, None, None), "st_layout_query")
+        self.S = int(S.value)
+        self.D = len(lens)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def offsets(self):
+        lib = load()
+        off = (_I64 * (self.D + 1))()
+        _check(lib.st_layout_query(self._h, None, off, None, None, None), "st_layout_query")
+        return [int(x) for x in off]
+
+    def positions(self):
+        lib = load()
+        pos = (_I64 * self.S)()
+        _check(lib.st_layout_query(self._h, None, None, pos, None, None), "st_layout_query")
+        return list(pos)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            load().st_layout_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected a [B, S, H, d] tensor")
+    return tuple(int(x) for x in q.shape)
+
+
+def _check_tensor(t, shape, dtype, name):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError("%s must be contiguous %s of shape %s" % (name, dtype, tuple(shape)))
+
+
+def st_attn_workspace_size(layout, B, H, d, dtype, pass_):
+    n = _SZ()
+    _check(load().st_attn_workspace_size(layout.handle, B, H, d, _dtype_code(dtype), pass_,
+                                         ctypes.byref(n)), "st_attn_workspace_size")
+    return int(n.value)
+
+
+def st_attn_fwd(layout, q, k, v, causal=False, scale=0.0, out=None, lse=None, stream=None):
+    """out, lse = attention of buffer-order BSHD q, k, v under ``layout``."""
+    B, S, H, d = _shape(q)
+    for t, n in ((k, "k"), (v, "v")):
+        _check_tensor(t, q.shape, q.dtype, n)
+    _check_tensor(q, q.shape, q.dtype, "q")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    _check_tensor(out, q.shape, q.dtype, "out")
+    _check_tensor(lse, (B, H, S), torch.float32, "lse")
+    _check(load().st_attn_fwd(layout.handle, B, H, d, _dtype_code(q.dtype), int(bool(causal)),
+                              float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                              None, 0, _stream(stream)), "st_attn_fwd")
+    return out, lse
+
+
+def st_attn_fwd_partials(layout, q, k, v, causal=False, scale=0.0, stream=None):
+    """Per-KV-shard partials: (partial_out [D,B,S,H,d] fp32, partial_lse [D,B,H,S])."""
+    B, S, H, d = _shape(q)
+    D = layout.D
+    po = torch.empty((D, B, S, H, d), device=q.device, dtype=torch.float32)
+    pl = torch.empty((D, B, H, S), device=q.device, dtype=torch.float32)
+    _check(load().st_attn_fwd_partials(layout.handle, B, H, d, _dtype_code(q.dtype),
+                                       int(bool(causal)), float(scale), _ptr(q), _ptr(k), _ptr(v),
+                                       _ptr(po), _ptr(pl), _stream(stream)), "st_attn_fwd_partials")
+    return po, pl
+
+
+def st_attn_merge(partial_out, partial_lse, out_dtype=torch.float32, out=None, lse=None,
+                  stream=None):
+    """Log-sum-exp merge of D partials -> (out [B,S,H,d], lse [B,H,S])."""
+    D, B, S, H, d = (int(x) for x in partial_out.shape)
+    _check_tensor(partial_out, (D, B, S, H, d), torch.float32, "partial_out")
+    _check_tensor(partial_lse, (D, B, H, S), torch.float32, "partial_lse")
+    if out is None:
+        out = torch.empty((B, S, H, d), device=partial_out.device, dtype=out_dtype)
+    if lse is None:
+        lse = torch.empty((B, H, S), device=partial_out.device, dtype=torch.float32)
+    _check(load().st_attn_merge(D, B, H, S, d, _ptr(partial_out), _ptr(partial_lse), _ptr(out),
+                                _ptr(lse), _dtype_code(out.dtype), _stream(stream)), "st_attn_merge")
+    return out, lse
+
+
+def st_attn_bwd(layout, q, k, v, out, lse, dout, causal=False, scale=0.0, grad_dtype=None,
+                workspace=None, stream=None):
+    """dq, dk, dv of sum(dout * out), in ``grad_dtype`` (default: fp32)."""
+    B, S, H, d = _shape(q)
+    for t, n in ((k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _check_tensor(t, q.shape, q.dtype, n)
+    _check_tensor(lse, (B, H, S), torch.float32, "lse")
+    need = st_attn_workspace_size(layout, B, H, d, q.dtype, 1)
+    if workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    gdt = torch.float32 if grad_dtype is None else grad_dtype
+    dq, dk, dv = (torch.empty(q.shape, device=q.device, dtype=gdt) for _ in range(3))
+    _check(load().st_attn_bwd(layout.handle, B, H, d, _dtype_code(q.dtype), int(bool(causal)),
+                              float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                              _ptr(dout), _dtype_code(gdt), _ptr(dq), _ptr(dk), _ptr(dv),
+                              _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream)),
+           "st_attn_bwd")
+    return dq, dk, dv
+
+
+def st_permute(layout, x, to_natural=True, stream=None):
+    B, S, H, d = _shape(x)
+    out = torch.empty_like(x)
+    _check(load().st_permute(layout.handle, B, H, d, _dtype_code(x.dtype), int(bool(to_natural)),
+                             _ptr(x), _ptr(out), _stream(stream)), "st_permute")
+    return out

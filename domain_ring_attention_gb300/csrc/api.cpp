@@ -1,0 +1,178 @@
+// C-ABI entry points: argument validation and dispatch to the kernels.
+// Every check happens on the host before anything is launched, so an invalid
+// call returns an error code and never reaches the GPU.
+#include <cmath>
+#include <cstdint>
+
+#include <cuda_runtime_api.h>
+
+#include "common.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_status(int err) {
+    if (err == 0) return ST_OK;
+    g_last_cuda_error = err;
+    return ST_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(const st_layout_t* L, int B, int H, int d, int dtype, float* scale) {
+    if (!L) return ST_ERR_NULL;
+    if (B < 1 || H < 1 || (int64_t)B * H > 65535) return ST_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ST_ERR_UNSUPPORTED;
+    if (dtype != ST_DTYPE_F32 && dtype != ST_DTYPE_BF16) return ST_ERR_UNSUPPORTED;
+    if (!std::isfinite(*scale)) return ST_ERR_INVALID_ARG;
+    if (*scale <= 0.f) *scale = 1.0f / std::sqrt((float)d);
+    return ST_OK;
+}
+
+}  // namespace
+
+extern "C" const char* st_error_string(int code) {
+    switch (code) {
+        case ST_OK: return "ok";
+        case ST_ERR_NULL: return "a required pointer is NULL";
+        case ST_ERR_INVALID_LAYOUT: return "invalid sharding shapes (D, a length < 1, or an odd zigzag length)";
+        case ST_ERR_UNSUPPORTED: return "unsupported head_dim or dtype";
+        case ST_ERR_MISALIGNED: return "a tensor pointer is not 16-byte aligned";
+        case ST_ERR_WORKSPACE: return "workspace missing or too small";
+        case ST_ERR_CUDA: return "CUDA error (see st_last_cuda_error)";
+        case ST_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
+        case ST_ERR_INVALID_ARG: return "an argument is out of range";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int st_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" int st_attn_workspace_size(const st_layout_t* L, int B, int H, int d, int dtype,
+                                      int pass, size_t* bytes) {
+    float scale = 1.f;
+    if (!bytes) return ST_ERR_NULL;
+    const int rc = check_common(L, B, H, d, dtype, &scale);
+    if (rc != ST_OK) return rc;
+    if (pass == 0) {
+        *bytes = 0;
+    } else if (pass == 1) {
+        const size_t rows = (size_t)B * (size_t)L->S * (size_t)H;
+        const size_t acc = rows * (size_t)d * sizeof(float);
+        // dq_acc then Delta, each 256-byte aligned
+        *bytes = ((acc + 255) & ~(size_t)255) + ((rows * sizeof(float) + 255) & ~(size_t)255);
+    } else {
+        return ST_ERR_INVALID_ARG;
+    }
+    return ST_OK;
+}
+
+extern "C" int st_attn_fwd(const st_layout_t* L, int B, int H, int d, int dtype, int causal,
+                           float scale, const void* q, const void* k, const void* v, void* out,
+                           float* lse, void* workspace, size_t ws_bytes, void* stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    int rc = check_common(L, B, H, d, dtype, &scale);
+    if (rc != ST_OK) return rc;
+    if (!q || !k || !v || !out || !lse) return ST_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+        return ST_ERR_MISALIGNED;
+    st::AttnArgs a{q, k, v, out, lse, nullptr, nullptr, B, H, d, causal ? 1 : 0, scale};
+    if (dtype == ST_DTYPE_BF16) {
+        bool handled = false;
+        rc = st::launch_fwd_tc(*L, a, stream, &handled);
+        if (handled) return cuda_status(rc);
+    }
+    st::SegTable t;
+    st::fill_segtable(*L, 64, &t);
+    return cuda_status(st::launch_fwd_simt(t, a, dtype, stream));
+}
+
+extern "C" int st_attn_fwd_partials(const st_layout_t* L, int B, int H, int d, int dtype,
+                                    int causal, float scale, const void* q, const void* k,
+                                    const void* v, float* partial_out, float* partial_lse,
+                                    void* stream) {
+    int rc = check_common(L, B, H, d, dtype, &scale);
+    if (rc != ST_OK) return rc;
+    if (!q || !k || !v || !partial_out || !partial_lse) return ST_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(partial_out) ||
+        !aligned16(partial_lse))
+        return ST_ERR_MISALIGNED;
+    st::AttnArgs a{q, k, v, nullptr, nullptr, partial_out, partial_lse, B, H, d, causal ? 1 : 0, scale};
+    st::SegTable t;
+    st::fill_segtable(*L, 64, &t);
+    return cuda_status(st::launch_fwd_simt(t, a, dtype, stream));
+}
+
+extern "C" int st_attn_merge(int D, int B, int H, int64_t S, int d, const float* partial_out,
+                             const float* partial_lse, void* out, float* lse, int out_dtype,
+                             void* stream) {
+    if (!partial_out || !partial_lse || !out || !lse) return ST_ERR_NULL;
+    if (D < 1 || D > ST_MAX_SHARDS || B < 1 || H < 1 || S < 1 || S >= INT32_MAX)
+        return ST_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ST_ERR_UNSUPPORTED;
+    if (out_dtype != ST_DTYPE_F32 && out_dtype != ST_DTYPE_BF16) return ST_ERR_UNSUPPORTED;
+    if (!aligned16(partial_out) || !aligned16(partial_lse) || !aligned16(out) || !aligned16(lse))
+        return ST_ERR_MISALIGNED;
+    return cuda_status(st::launch_merge(D, B, H, S, d, partial_out, partial_lse, out, lse,
+                                        out_dtype, stream));
+}
+
+extern "C" int st_attn_bwd(const st_layout_t* L, int B, int H, int d, int dtype, int causal,
+                           float scale, const void* q, const void* k, const void* v,
+                           const void* out, const float* lse, const void* dout, int grad_dtype,
+                           void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                           void* stream) {
+    int rc = check_common(L, B, H, d, dtype, &scale);
+    if (rc != ST_OK) return rc;
+    if (grad_dtype != ST_DTYPE_F32 && grad_dtype != dtype) return ST_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return ST_ERR_NULL;
+    const void* ptrs[] = {q, k, v, out, lse, dout, dq, dk, dv};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return ST_ERR_MISALIGNED;
+    size_t need = 0;
+    rc = st_attn_workspace_size(L, B, H, d, dtype, 1, &need);
+    if (rc != ST_OK) return rc;
+    if (!workspace || ws_bytes < need) return ST_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ST_ERR_MISALIGNED;
+    const size_t rows = (size_t)B * (size_t)L->S * (size_t)H;
+    const size_t acc_bytes = (rows * (size_t)d * sizeof(float) + 255) & ~(size_t)255;
+    // fp32 gradients accumulate straight into dq; otherwise into the workspace
+    float* dq_acc = grad_dtype == ST_DTYPE_F32 ? static_cast<float*>(dq) : static_cast<float*>(workspace);
+    float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes);
+    st::BwdArgs a{q, k, v, out, lse, dout, dq, dk, dv, dq_acc, delta, B, H, d, causal ? 1 : 0,
+                  scale, grad_dtype};
+    cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+
+    rc = cuda_status((int)cudaMemsetAsync(dq_acc, 0, rows * (size_t)d * sizeof(float), st_));
+    if (rc != ST_OK) return rc;
+    rc = cuda_status(st::launch_bwd_preprocess(a, L->S, dtype, stream));
+    if (rc != ST_OK) return rc;
+    bool handled = false;
+    if (dtype == ST_DTYPE_BF16) {
+        rc = st::launch_bwd_tc(*L, a, stream, &handled);
+        if (handled && rc != 0) return cuda_status(rc);
+    }
+    if (!handled) {
+        st::SegTable t;
+        st::fill_segtable(*L, 64, &t);
+        rc = cuda_status(st::launch_bwd_simt(t, a, dtype, stream));
+        if (rc != ST_OK) return rc;
+    }
+    if (grad_dtype == ST_DTYPE_F32) return ST_OK;
+    return cuda_status(st::launch_dq_convert(a, L->S, grad_dtype, stream));
+}
+
+extern "C" int st_permute(const st_layout_t* L, int B, int H, int d, int dtype, int to_natural,
+                          const void* in, void* out, void* stream) {
+    float scale = 1.f;
+    int rc = check_common(L, B, H, d, dtype, &scale);
+    if (rc != ST_OK) return rc;
+    if (!in || !out) return ST_ERR_NULL;
+    if (in == out) return ST_ERR_INVALID_ARG;
+    if (!aligned16(in) || !aligned16(out)) return ST_ERR_MISALIGNED;
+    st::SegTable t;
+    st::fill_segtable(*L, 64, &t);
+    return cuda_status(st::launch_permute(t, B, H, d, dtype, to_natural ? 1 : 0, in, out, stream));
+}

@@ -1,0 +1,204 @@
+// Bandwidth-bound helper kernels: the standalone log-sum-exp merge, the
+// backward row sums Delta, the dQ accumulator conversion and the
+// buffer <-> natural row permutation.
+//
+// All four stream rows of d contiguous elements: one warp per row, lanes
+// moving consecutive 8/16-byte pieces, grid-stride loops over rows with the
+// grid sized to a multiple of the SM count.
+#include <cmath>
+
+#include "device.cuh"
+
+namespace st {
+namespace {
+
+constexpr int kWarps = 8;
+
+int grid_for(int64_t rows) {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    const int64_t want = (rows + kWarps - 1) / kWarps;
+    const int64_t cap = (int64_t)sms * 16;
+    return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+// Log-sum-exp merge (ring-attention combine): L = log sum_j exp(lse_j),
+// out = sum_j exp(lse_j - L) O_j; every lse_j = -inf gives L = -inf, out = 0.
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarps * 32)
+merge_kernel(int nparts, int B, int H, int S, const float* __restrict__ part_out,
+             const float* __restrict__ part_lse, T* __restrict__ out, float* __restrict__ lse) {
+    constexpr int PER = D / 32;   // elements per lane (2 or 4)
+    const int lane = threadIdx.x & 31;
+    const int64_t nrows = (int64_t)B * S * H;
+    const int64_t elems = nrows * D;
+    const int64_t lse_n = (int64_t)B * H * S;
+    for (int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); row < nrows;
+         row += (int64_t)gridDim.x * kWarps) {
+        const int h = (int)(row % H);
+        const int64_t bs = row / H;
+        const int s = (int)(bs % S);
+        const int b = (int)(bs / S);
+        const int64_t li = ((int64_t)b * H + h) * S + s;
+        float m = -INFINITY;
+        for (int j = 0; j < nparts; ++j) m = fmaxf(m, part_lse[j * lse_n + li]);
+        float acc[PER];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+        float tot = 0.f;
+        if (m != -INFINITY) {
+            for (int j = 0; j < nparts; ++j) {
+                const float w = expf(part_lse[j * lse_n + li] - m);
+                tot += w;
+                const float* src = part_out + j * elems + row * D + lane * PER;
+                if constexpr (PER == 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(src);
+                    acc[0] = fmaf(w, x.x, acc[0]);
+                    acc[1] = fmaf(w, x.y, acc[1]);
+                    acc[PER - 2] = fmaf(w, x.z, acc[PER - 2]);
+                    acc[PER - 1] = fmaf(w, x.w, acc[PER - 1]);
+                } else {
+                    const float2 x = *reinterpret_cast<const float2*>(src);
+                    acc[0] = fmaf(w, x.x, acc[0]);
+                    acc[1] = fmaf(w, x.y, acc[1]);
+                }
+            }
+        }
+        const float inv = tot > 0.f ? 1.f / tot : 0.f;
+        T* dst = out + row * D + lane * PER;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) dst[e] = from_f32<T>(acc[e] * inv);
+        if (lane == 0) lse[li] = tot > 0.f ? m + logf(tot) : -INFINITY;
+    }
+}
+
+// Delta_i = sum_c dO_ic * O_ic in fp32 (backward preprocess).
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarps * 32)
+delta_kernel(int B, int H, int S, const T* __restrict__ o, const T* __restrict__ dout,
+             float* __restrict__ delta) {
+    constexpr int PER = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t nrows = (int64_t)B * S * H;
+    for (int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); row < nrows;
+         row += (int64_t)gridDim.x * kWarps) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            const int64_t i = row * D + lane * PER + e;
+            acc = fmaf(to_f32(o[i]), to_f32(dout[i]), acc);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) {
+            const int h = (int)(row % H);
+            const int64_t bs = row / H;
+            const int s = (int)(bs % S);
+            const int b = (int)(bs / S);
+            delta[((int64_t)b * H + h) * S + s] = acc;
+        }
+    }
+}
+
+template <typename T>
+__global__ void convert_kernel(int64_t n, const float* __restrict__ src, T* __restrict__ dst) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = from_f32<T>(src[i]);
+}
+
+// Row permutation between buffer order and natural order, 16-byte pieces.
+__global__ void __launch_bounds__(kWarps * 32)
+permute_kernel(const __grid_constant__ SegTable tab, int B, int H, int row_bytes,
+               int to_natural, const uint4* __restrict__ in, uint4* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int pieces = row_bytes / 16;
+    const int S = tab.S;
+    const int64_t nrows = (int64_t)B * S;
+    for (int64_t bt = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); bt < nrows;
+         bt += (int64_t)gridDim.x * kWarps) {
+        const int t = (int)(bt % S);
+        const int64_t b = bt / S;
+        int s = 0;
+        while (s + 1 < tab.nseg && tab.seg_buf[s + 1] <= t) ++s;
+        const int p = tab.seg_nat[s] + (t - tab.seg_buf[s]);
+        const int64_t src_row = b * S + (to_natural ? t : p);
+        const int64_t dst_row = b * S + (to_natural ? p : t);
+        const int64_t per_tok = (int64_t)H * pieces;
+        for (int64_t i = lane; i < per_tok; i += 32) out[dst_row * per_tok + i] = in[src_row * per_tok + i];
+    }
+}
+
+}  // namespace
+
+int launch_merge(int D, int B, int H, int64_t S, int d, const float* part_out,
+                 const float* part_lse, void* out, float* lse, int out_dtype, void* stream) {
+    const int64_t rows = (int64_t)B * S * H;
+    const int grid = grid_for(rows);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (out_dtype == ST_DTYPE_F32) {
+        if (d == 64)
+            merge_kernel<float, 64><<<grid, kWarps * 32, 0, st>>>(D, B, H, (int)S, part_out, part_lse,
+                                                                  static_cast<float*>(out), lse);
+        else
+            merge_kernel<float, 128><<<grid, kWarps * 32, 0, st>>>(D, B, H, (int)S, part_out, part_lse,
+                                                                   static_cast<float*>(out), lse);
+    } else {
+        if (d == 64)
+            merge_kernel<__nv_bfloat16, 64><<<grid, kWarps * 32, 0, st>>>(
+                D, B, H, (int)S, part_out, part_lse, static_cast<__nv_bfloat16*>(out), lse);
+        else
+            merge_kernel<__nv_bfloat16, 128><<<grid, kWarps * 32, 0, st>>>(
+                D, B, H, (int)S, part_out, part_lse, static_cast<__nv_bfloat16*>(out), lse);
+    }
+    return (int)cudaGetLastError();
+}
+
+int launch_bwd_preprocess(const BwdArgs& a, int64_t S, int dtype, void* stream) {
+    const int64_t rows = (int64_t)a.B * S * a.H;
+    const int grid = grid_for(rows);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == ST_DTYPE_F32) {
+        auto o = static_cast<const float*>(a.out);
+        auto g = static_cast<const float*>(a.dout);
+        if (a.d == 64)
+            delta_kernel<float, 64><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
+        else
+            delta_kernel<float, 128><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
+    } else {
+        auto o = static_cast<const __nv_bfloat16*>(a.out);
+        auto g = static_cast<const __nv_bfloat16*>(a.dout);
+        if (a.d == 64)
+            delta_kernel<__nv_bfloat16, 64><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
+        else
+            delta_kernel<__nv_bfloat16, 128><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
+    }
+    return (int)cudaGetLastError();
+}
+
+int launch_dq_convert(const BwdArgs& a, int64_t S, int dtype, void* stream) {
+    const int64_t n = (int64_t)a.B * S * a.H * a.d;
+    const int grid = grid_for(n / 32 + 1);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == ST_DTYPE_F32)
+        convert_kernel<float><<<grid, 256, 0, st>>>(n, a.dq_acc, static_cast<float*>(a.dq));
+    else
+        convert_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(n, a.dq_acc, static_cast<__nv_bfloat16*>(a.dq));
+    return (int)cudaGetLastError();
+}
+
+int launch_permute(const SegTable& t, int B, int H, int d, int dtype, int to_natural,
+                   const void* in, void* out, void* stream) {
+    const int row_bytes = d * (dtype == ST_DTYPE_F32 ? 4 : 2);
+    const int64_t rows = (int64_t)B * t.S;
+    permute_kernel<<<grid_for(rows), kWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        t, B, H, row_bytes, to_natural, static_cast<const uint4*>(in), static_cast<uint4*>(out));
+    return (int)cudaGetLastError();
+}
+
+}  // namespace st

@@ -1,0 +1,89 @@
+// Internal declarations shared by the host layout code, the C-ABI layer and
+// the kernels.  Not part of the public interface (include/st_attn.h is).
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "st_attn.h"
+
+// Host-resident layout descriptor behind the opaque st_layout_t.
+//
+// A *segment* is a maximal run of buffer rows whose natural positions are
+// consecutive.  Without zigzag the segments are the shards; with zigzag shard
+// r contributes two segments (natural chunks r and 2D-1-r, in that order).
+struct st_layout {
+    int D = 0;
+    int zigzag = 0;
+    int64_t S = 0;
+    std::vector<int64_t> lens;       // D sharding shapes
+    std::vector<int64_t> off;        // D+1 prefix offsets
+    std::vector<int64_t> seg_buf;    // nseg+1 buffer starts (last = S)
+    std::vector<int64_t> seg_nat;    // nseg natural start positions
+    std::vector<int> shard_seg;      // D+1: shard r owns segments [shard_seg[r], shard_seg[r+1])
+};
+
+namespace st {
+
+constexpr int kMaxSegs = 2 * ST_MAX_SHARDS;
+
+// The layout as kernels see it: a by-value kernel parameter (no device
+// allocation), plus the per-segment tile prefix for the launch's tile height.
+struct SegTable {
+    int32_t nseg;
+    int32_t D;
+    int32_t S;
+    int32_t ntiles;                       // query tiles per (b, h)
+    int32_t seg_buf[kMaxSegs + 1];
+    int32_t seg_nat[kMaxSegs];
+    int32_t seg_tile[kMaxSegs + 1];       // exclusive prefix of tiles per segment
+    int32_t shard_seg[ST_MAX_SHARDS + 1];
+};
+
+void fill_segtable(const st_layout& L, int tile_rows, SegTable* t);
+
+// Arguments common to the attention kernels.
+struct AttnArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;            // forward output (input dtype) or nullptr
+    float* lse;           // [B,H,S]
+    float* part_out;      // partials mode: [D,B,S,H,d] fp32, else nullptr
+    float* part_lse;      // partials mode: [D,B,H,S] fp32
+    int B, H, d;
+    int causal;
+    float scale;          // 1/sqrt(d) unless the caller chose another
+};
+
+struct BwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* out;
+    const float* lse;
+    const void* dout;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* dq_acc;        // [B,S,H,d] fp32 accumulator (dq itself for fp32 gradients)
+    float* delta;         // [B,H,S] fp32 workspace
+    int B, H, d;
+    int causal;
+    float scale;
+    int grad_dtype;       // dtype of dq, dk, dv
+};
+
+// ---- launchers (return a cudaError_t value; 0 = success) ----
+int launch_fwd_simt(const SegTable& t, const AttnArgs& a, int dtype, void* stream);
+int launch_fwd_tc(const st_layout& L, const AttnArgs& a, void* stream, bool* handled);
+int launch_bwd_simt(const SegTable& t, const BwdArgs& a, int dtype, void* stream);
+int launch_bwd_tc(const st_layout& L, const BwdArgs& a, void* stream, bool* handled);
+int launch_merge(int D, int B, int H, int64_t S, int d, const float* part_out,
+                 const float* part_lse, void* out, float* lse, int out_dtype, void* stream);
+int launch_bwd_preprocess(const BwdArgs& a, int64_t S, int dtype, void* stream);
+int launch_dq_convert(const BwdArgs& a, int64_t S, int dtype, void* stream);
+int launch_permute(const SegTable& t, int B, int H, int d, int dtype, int to_natural,
+                   const void* in, void* out, void* stream);
+
+}  // namespace st

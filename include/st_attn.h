@@ -1,0 +1,162 @@
+/*
+ * st_attn.h -- sharded ring attention on one GPU (GB300, sm_103a).
+ *
+ * Attention over a sequence that is split into D shards of arbitrary lengths
+ * ("sharding shapes": ShardTensor summary, section 2, a fourth metadata item
+ * giving each rank's local chunk shape along the sharded axis), computed the
+ * ring-attention way (ShardTensor summary, section 4, ring attention): every
+ * query shard meets every KV shard in turn and the partial results are merged
+ * with the log-sum-exp rule.  An optional zigzag re-partition (TSP summary,
+ * "Folding Tensor and Sequence Parallelism", section 2, attention layer) cuts
+ * the sequence into 2D chunks and gives rank r chunks r and 2D-1-r so causal
+ * work is balanced.
+ *
+ * On one GPU the D shards are row ranges of one HBM buffer and the "ring" is
+ * the kernel's loop over KV shards: no collectives are involved.
+ *
+ * Conventions shared by every call:
+ *   - Tensors q, k, v, out, dout, dq, dk, dv are BSHD: [B, S, H, d], row-major
+ *     and contiguous, in *buffer order*: shard 0's rows, then shard 1's, ...
+ *     With zigzag, shard r's slab is [chunk r ; chunk 2D-1-r] (natural order
+ *     chunk lengths c_r = c_{2D-1-r} = L_r / 2).
+ *   - lse is [B, H, S] fp32, natural logarithm of sum_j exp(scale * q.k_j).
+ *   - "causal" masks by *natural* sequence position: query i sees key j iff
+ *     pos(j) <= pos(i).  Without causal every query sees every key.
+ *   - scale <= 0 selects 1/sqrt(d).
+ *   - dtype: ST_DTYPE_F32 (fp32 in and out, fp32 SIMT arithmetic) or
+ *     ST_DTYPE_BF16 (bf16 in and out, tensor cores, fp32 accumulation).
+ *     lse and all accumulators are fp32.
+ *   - d (head_dim) is 64 or 128.
+ *   - Pointers named q, k, ... are DEVICE pointers that the caller owns and
+ *     keeps alive until the work on `stream` has finished; they must be
+ *     16-byte aligned.  `stream` is a cudaStream_t (NULL = legacy default
+ *     stream).  All GPU work is asynchronous on that stream.
+ *   - No call allocates device memory.  Scratch that a call needs is a
+ *     caller-provided workspace whose size st_attn_workspace_size reports.
+ *   - Every call returns ST_OK (0) or a negative ST_ERR_* code; no call aborts
+ *     the process or traps the GPU.  On ST_ERR_CUDA, st_last_cuda_error()
+ *     returns the CUDA runtime error code that caused it.
+ */
+#ifndef ST_ATTN_H
+#define ST_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    ST_OK = 0,
+    ST_ERR_NULL = -1,            /* a required pointer is NULL                      */
+    ST_ERR_INVALID_LAYOUT = -2,  /* D out of range, a length < 1, odd zigzag length */
+    ST_ERR_UNSUPPORTED = -3,     /* head_dim or dtype not supported                 */
+    ST_ERR_MISALIGNED = -4,      /* a tensor pointer is not 16-byte aligned         */
+    ST_ERR_WORKSPACE = -5,       /* workspace NULL or smaller than required         */
+    ST_ERR_CUDA = -6,            /* a CUDA runtime call or launch failed            */
+    ST_ERR_DEVICE_TIMEOUT = -7,  /* a bounded device-side wait gave up              */
+    ST_ERR_INVALID_ARG = -8      /* B, H, S, D or another size is out of range      */
+};
+
+enum { ST_DTYPE_F32 = 0, ST_DTYPE_BF16 = 1 };
+
+enum { ST_MAX_SHARDS = 32 };
+
+/* Opaque, host-resident shard-layout descriptor.  Thread-safe to read from
+ * several host threads at once; create and destroy are not synchronised. */
+typedef struct st_layout st_layout_t;
+
+/* Build a layout from the sharding shapes (ShardTensor summary, section 2).
+ *   shard_lens : host array of D lengths L_0..L_{D-1}, each >= 1 (even when
+ *                zigzag != 0).  S = sum L_r must be < 2^31.
+ *   D          : 1 .. ST_MAX_SHARDS.
+ *   zigzag     : 0 = contiguous shards; 1 = zigzag re-partition (TSP summary,
+ *                section 2): rank r holds natural chunks r and 2D-1-r.
+ *   out        : receives a new descriptor owned by the caller
+ *                (free it with st_layout_destroy).
+ * Errors: ST_ERR_NULL, ST_ERR_INVALID_LAYOUT.  Host only; no CUDA calls. */
+int st_layout_create(const int64_t* shard_lens, int D, int zigzag, st_layout_t** out);
+
+/* Free a descriptor from st_layout_create.  NULL is accepted. */
+int st_layout_destroy(st_layout_t* layout);
+
+/* Read back the layout (host arrays, any of them may be NULL):
+ *   S       : total rows.
+ *   offsets : D+1 prefix offsets, offsets[r] = first buffer row of shard r.
+ *   pos     : S natural positions, pos[t] = sequence position of buffer row t.
+ *   D, zigzag : the creation arguments. */
+int st_layout_query(const st_layout_t* layout, int64_t* S, int64_t* offsets, int64_t* pos,
+                    int* D, int* zigzag);
+
+/* Workspace bytes needed by st_attn_fwd (pass = 0) or st_attn_bwd (pass = 1)
+ * for these sizes.  The forward needs none (the merge is fused); the backward
+ * needs an fp32 dQ accumulator [B,S,H,d] and the row sums Delta [B,H,S]. */
+int st_attn_workspace_size(const st_layout_t* layout, int B, int H, int d, int dtype,
+                           int pass, size_t* bytes);
+
+/* Forward: out = softmax(scale * Q K^T, masked) V and lse, ring order.
+ * Each query tile visits KV shards r, r-1, ..., r+1 (mod D) where r is its
+ * own shard -- the order in which rank r receives K/V around a ring -- and
+ * folds every KV tile into a running (max, sum, O) state, which is the
+ * log-sum-exp merge of the per-shard partials carried out incrementally.
+ *   q, k, v : [B,S,H,d] input dtype;  out : [B,S,H,d] input dtype;
+ *   lse     : [B,H,S] fp32 (may not be NULL).
+ *   workspace, ws_bytes : unused by the forward (may be NULL / 0). */
+int st_attn_fwd(const st_layout_t* layout, int B, int H, int d, int dtype, int causal,
+                float scale, const void* q, const void* k, const void* v, void* out,
+                float* lse, void* workspace, size_t ws_bytes, void* stream);
+
+/* Forward that stops short of the merge: for every query row and every KV
+ * shard j it writes the partial (O_j normalised by its own sum, lse_j) over
+ * the keys of shard j only -- what each ring step would hand to the merge.
+ * A partial with no visible key has O_j = 0 and lse_j = -inf.
+ *   partial_out : [D,B,S,H,d] fp32;  partial_lse : [D,B,H,S] fp32.
+ * st_attn_merge of these partials equals st_attn_fwd up to rounding. */
+int st_attn_fwd_partials(const st_layout_t* layout, int B, int H, int d, int dtype,
+                         int causal, float scale, const void* q, const void* k,
+                         const void* v, float* partial_out, float* partial_lse,
+                         void* stream);
+
+/* Log-sum-exp merge of D partials (the ring-attention combine step):
+ *   L = log sum_j exp(lse_j);  out = sum_j exp(lse_j - L) O_j.
+ * All-(-inf) rows give L = -inf and out = 0.
+ *   partial_out : [D,B,S,H,d] fp32;  partial_lse : [D,B,H,S] fp32;
+ *   out : [B,S,H,d] out_dtype;  lse : [B,H,S] fp32.   d in {64, 128}. */
+int st_attn_merge(int D, int B, int H, int64_t S, int d, const float* partial_out,
+                  const float* partial_lse, void* out, float* lse, int out_dtype,
+                  void* stream);
+
+/* Backward of st_attn_fwd: given out and lse saved by the forward and the
+ * output gradient dout, writes dq, dk, dv ([B,S,H,d], all three in grad_dtype).
+ * With P = exp(scale*QK^T - lse): dV = P^T dO; dP = dO V^T;
+ * Delta = rowsum(dO * out); dS = P * (dP - Delta); dQ = scale dS K;
+ * dK = scale dS^T Q.
+ *   q, k, v, out, dout : input dtype;  lse : [B,H,S] fp32 from the forward.
+ *   grad_dtype : ST_DTYPE_F32 (fp32 gradients, no final rounding) or the
+ *                input dtype.
+ *   workspace  : at least st_attn_workspace_size(pass=1) bytes of device
+ *                memory, 16-byte aligned; its contents on entry do not matter.
+ * Errors: as st_attn_fwd, plus ST_ERR_WORKSPACE. */
+int st_attn_bwd(const st_layout_t* layout, int B, int H, int d, int dtype, int causal,
+                float scale, const void* q, const void* k, const void* v,
+                const void* out, const float* lse, const void* dout, int grad_dtype,
+                void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream);
+
+/* Reorder rows between buffer order and natural sequence order:
+ *   to_natural = 1 : out[:, pos(t)] = in[:, t]   (buffer -> natural)
+ *   to_natural = 0 : out[:, t] = in[:, pos(t)]   (natural -> buffer)
+ * in/out : [B,S,H,d] dtype, distinct buffers. */
+int st_permute(const st_layout_t* layout, int B, int H, int d, int dtype, int to_natural,
+               const void* in, void* out, void* stream);
+
+/* Human-readable text for a status code (static storage). */
+const char* st_error_string(int code);
+
+/* CUDA runtime error code behind the most recent ST_ERR_CUDA of this thread. */
+int st_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ST_ATTN_H */

@@ -1,0 +1,115 @@
+"""CPU-only checks of the C-ABI library: it loads, exports every symbol the
+header declares, builds layouts that agree with the oracle's layout, and
+rejects bad arguments with error codes before touching a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import domain_ring_attention_gb300 as st
+from domain_ring_attention_gb300 import _lib
+from oracle import layout as ol
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", f)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names.update(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(st_\w+)\s*\(", txt, flags=re.M))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        from domain_ring_attention_gb300 import build
+        build.build()
+    return st.load()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert "st_attn_fwd" in names and "st_layout_create" in names and len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert {p[0] for p in _lib.PROTOTYPES} == set(names)
+
+
+@pytest.mark.parametrize("lens,zigzag", [
+    ([100, 150, 130, 132], False), ([16384] * 8, True), ([12928, 19392, 384, 64], True),
+    ([2], True), ([1], False), ([7, 1, 3], False), ([2] * 32, True)])
+def test_layout_matches_oracle(lib, lens, zigzag):
+    lay = st.Layout(lens, zigzag)
+    assert lay.S == sum(lens)
+    assert lay.offsets() == list(ol.shard_offsets(lens))
+    assert np.array_equal(np.array(lay.positions()), ol.natural_positions(lens, zigzag))
+
+
+@pytest.mark.parametrize("lens,zigzag", [([], False), ([3, 0], False), ([3, 4], True),
+                                         ([1] * 33, False), ([-2], False)])
+def test_layout_rejects_bad_shapes(lib, lens, zigzag):
+    arr = (ctypes.c_int64 * max(1, len(lens)))(*lens)
+    h = ctypes.c_void_p()
+    rc = lib.st_layout_create(arr, len(lens), int(zigzag), ctypes.byref(h))
+    assert rc == -2 and not h.value
+
+
+def test_layout_null_and_bad_flag(lib):
+    h = ctypes.c_void_p()
+    assert lib.st_layout_create(None, 1, 0, ctypes.byref(h)) == -1
+    arr = (ctypes.c_int64 * 1)(4)
+    assert lib.st_layout_create(arr, 1, 2, ctypes.byref(h)) == -8
+    assert lib.st_layout_destroy(None) == 0
+
+
+def test_workspace_sizes(lib):
+    lay = st.Layout([100, 150, 130, 132])
+    n = ctypes.c_size_t()
+    assert lib.st_attn_workspace_size(lay.handle, 1, 2, 64, 0, 0, ctypes.byref(n)) == 0 and n.value == 0
+    assert lib.st_attn_workspace_size(lay.handle, 1, 2, 64, 0, 1, ctypes.byref(n)) == 0
+    rows = 512 * 2
+    assert n.value >= rows * 64 * 4 + rows * 4
+    assert lib.st_attn_workspace_size(lay.handle, 1, 2, 96, 0, 1, ctypes.byref(n)) == -3
+    assert lib.st_attn_workspace_size(lay.handle, 1, 2, 64, 7, 1, ctypes.byref(n)) == -3
+    assert lib.st_attn_workspace_size(lay.handle, 1, 2, 64, 0, 2, ctypes.byref(n)) == -8
+
+
+def test_bad_calls_return_codes_without_a_gpu(lib):
+    """Validation happens on the host, before any CUDA call."""
+    lay = st.Layout([64, 64])
+    P = ctypes.c_void_p
+    good = P(0x10000)
+    lse = P(0x20000)
+    fwd = lib.st_attn_fwd
+    assert fwd(None, 1, 1, 64, 1, 0, 0.0, good, good, good, good, lse, None, 0, None) == -1
+    assert fwd(lay.handle, 1, 1, 80, 1, 0, 0.0, good, good, good, good, lse, None, 0, None) == -3
+    assert fwd(lay.handle, 1, 1, 64, 5, 0, 0.0, good, good, good, good, lse, None, 0, None) == -3
+    assert fwd(lay.handle, 0, 1, 64, 1, 0, 0.0, good, good, good, good, lse, None, 0, None) == -8
+    assert fwd(lay.handle, 1, 1, 64, 1, 0, float("nan"), good, good, good, good, lse, None, 0, None) == -8
+    assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, None, good, good, good, lse, None, 0, None) == -1
+    assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, P(0x10008), good, good, good, lse, None, 0, None) == -4
+    bwd = lib.st_attn_bwd
+    args = [good] * 6
+    assert bwd(lay.handle, 1, 1, 64, 1, 0, 0.0, *args, 1, good, good, good, None, 0, None) == -5
+    assert bwd(lay.handle, 1, 1, 64, 1, 0, 0.0, *args, 1, good, good, good, good, 16, None) == -5
+    assert bwd(lay.handle, 1, 1, 64, 0, 0, 0.0, *args, 1, good, good, good, good, 1 << 30, None) == -3
+    mrg = lib.st_attn_merge
+    assert mrg(0, 1, 1, 64, 64, good, good, good, lse, 0, None) == -8
+    assert mrg(33, 1, 1, 64, 64, good, good, good, lse, 0, None) == -8
+    assert mrg(2, 1, 1, 64, 96, good, good, good, lse, 0, None) == -3
+    assert lib.st_permute(lay.handle, 1, 1, 64, 1, 1, good, good, None) == -8
+    assert lib.st_error_string(-4).decode().startswith("a tensor pointer")
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    import torch
+    lay = st.Layout([4, 4])
+    x = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        st.st_attn_fwd(lay, x, x, x)
