@@ -1,0 +1,326 @@
+"""Benchmark: sharded ring attention forward on one GB300 (and N replicas).
+
+Default workload: ViT-style 4096^2 image, patch 16 -> S = 65536 tokens,
+B=1, H=16, head_dim=64, bf16, D=16 equal shards, non-causal, forward only.
+A step is one st_attn_fwd call (layout + ring-order fused forward with the
+log-sum-exp merge) over inputs already resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+With N > 1 (torchrun, one rank per GPU) every rank runs the same workload on
+its own GPU with no data-path collective (weak scaling); value = total FLOPs of
+all ranks / the slowest rank's time.  ``--impl reference`` times the float64
+CPU oracle on a bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+from domain_ring_attention_gb300.workloads import WORKLOADS, make_inputs
+
+METRIC = "ring-attention fwd/bwd TFLOP/s (bf16, S=65536) and % of GB300 dense-BF16 peak"
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+# dram bytes (read + write) per launch of the forward kernel from the committed
+# ncu capture of the current kernel version; None when not captured for it.
+NCU_TRAFFIC_BYTES = {}
+KERNEL_VERSION = "fwd_tc_v1"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="vit4096_s65536", choices=sorted(WORKLOADS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args()
+
+
+def dist_init(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            m = json.load(open(path))
+            return (float(m.get("bf16_tflops")), float(m.get("bf16_tflops_sustained", m.get("bf16_tflops"))),
+                    float(m.get("hbm_gbs")), "measured")
+        except Exception:
+            pass
+    return FALLBACK_BF16_TFLOPS, 1700.0, FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        self.file.flush()
+        rows = [l.strip().split(",") for l in open(self.file.name) if l.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+                for name, val in zip(names, r[3:7]):
+                    if "Active" in val and "Not" not in val:
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_sample_tflops(wl, q, k, v, budget_s=12.0):
+    """The float64 oracle on a bounded, growing sample of query rows."""
+    from oracle import attention as oa
+    rng = np.random.default_rng(0)
+    S = wl.S
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    flops = 0.0
+    rows_done = 0
+    t0 = time.perf_counter()
+    it = 0
+    while time.perf_counter() - t0 < budget_s:
+        b, h = heads[it % len(heads)]
+        rows = np.sort(rng.choice(S, size=min(64, S), replace=False))
+        qh = q[b:b + 1, :, h:h + 1].float().numpy().astype(np.float64)
+        kh = k[b:b + 1, :, h:h + 1].float().numpy().astype(np.float64)
+        vh = v[b:b + 1, :, h:h + 1].float().numpy().astype(np.float64)
+        oa.forward_rows(qh, kh, vh, wl.lens, wl.zigzag, wl.causal, rows, heads=[(0, 0)])
+        vis = S if not wl.causal else (S + 1) / 2.0
+        flops += 4.0 * wl.d * vis * len(rows)
+        rows_done += len(rows)
+        it += 1
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return flops / dt / 1e12, rows_done, dt, cores
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]
+    g = torch.Generator().manual_seed(0)
+    shape = (wl.B, wl.S, wl.H, wl.d)
+    q, k, v = (torch.randn(shape, generator=g).to(wl.torch_dtype) for _ in range(3))
+    vals = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        val, rows, dt, cores = cpu_sample_tflops(wl, q, k, v, budget_s=2.0)
+        if i >= args.warmup:
+            vals.append(val)
+            info = (rows, dt, cores)
+    value = statistics.median(vals)
+    sample = "%d query rows per step over all heads, float64 numpy oracle" % info[0]
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": info[1] * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(wl.describe(), parallelism="replicas%d" % world),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": info[2], "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world):
+    import domain_ring_attention_gb300 as st
+    st.load()
+    wl = WORKLOADS[args.workload]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q_h, k_h, v_h = make_inputs(wl, seed=rank, device="cpu")
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    lay = st.Layout(wl.lens, wl.zigzag)
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.H, wl.S), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        st.st_attn_fwd(lay, q, k, v, causal=wl.causal, out=out, lse=lse, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        time.sleep(0.3)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_per_step = total_ms / args.steps
+    flops = wl.fwd_flops()
+    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    peak_b, peak_s, hbm, peak_kind = peaks()
+    achieved = flops / (statistics.mean(launch_ms) * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        pin = [x.pin_memory() for x in (q_h, k_h, v_h)]
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            qd.copy_(pin[0], non_blocking=True)
+            kd.copy_(pin[1], non_blocking=True)
+            vd.copy_(pin[2], non_blocking=True)
+            st.st_attn_fwd(lay, qd, kd, vd, causal=wl.causal, out=out, lse=lse, stream=stream)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, min(args.steps, 10))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world)
+        h2d = sum(x.numel() * x.element_size() for x in pin)
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+        e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        val, rows, dt, cores = cpu_sample_tflops(wl, q_h, k_h, v_h, budget_s=12.0)
+        cpu = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": "%d query rows (64 per head, cycling heads) of the same workload, "
+                         "float64 numpy, %.1f s" % (rows, dt)}
+
+    if rank == 0:
+        in_bytes = 3 * q.numel() * q.element_size()
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": dict(wl.describe(), parallelism="replicas%d" % world,
+                           l2="inputs %d MiB > 129 MB L2, no flush" % (in_bytes >> 20)),
+            "pct_of_peak": 100.0 * value / world / peak_b,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_b,
+                         "unit": "TFLOP/s", "frac": achieved / peak_b,
+                         "traffic": NCU_TRAFFIC_BYTES.get(KERNEL_VERSION),
+                         "peak_kind": peak_kind + " burst bf16"},
+            "gpu_launches": args.steps,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world = dist_init(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

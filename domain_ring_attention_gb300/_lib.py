@@ -45,6 +45,7 @@ PROTOTYPES = [
     ("st_permute", _I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     ("st_error_string", ctypes.c_char_p, [_I]),
     ("st_last_cuda_error", _I, []),
+    ("st_device_error", _I, [_P]),
 ]
 
 _lib = None

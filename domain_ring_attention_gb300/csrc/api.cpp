@@ -49,6 +49,15 @@ extern "C" const char* st_error_string(int code) {
 
 extern "C" int st_last_cuda_error(void) { return g_last_cuda_error; }
 
+extern "C" int st_device_error(void* stream) {
+    int rc = cuda_status((int)cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    if (rc != ST_OK) return rc;
+    const int f = st::fwd_tc_device_error(true);
+    const int b = st::bwd_tc_device_error(true);
+    if (f < 0 || b < 0) return cuda_status((int)cudaGetLastError());
+    return (f || b) ? ST_ERR_DEVICE_TIMEOUT : ST_OK;
+}
+
 extern "C" int st_attn_workspace_size(const st_layout_t* L, int B, int H, int d, int dtype,
                                       int pass, size_t* bytes) {
     float scale = 1.f;

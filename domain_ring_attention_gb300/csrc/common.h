@@ -79,6 +79,10 @@ int launch_fwd_simt(const SegTable& t, const AttnArgs& a, int dtype, void* strea
 int launch_fwd_tc(const st_layout& L, const AttnArgs& a, void* stream, bool* handled);
 int launch_bwd_simt(const SegTable& t, const BwdArgs& a, int dtype, void* stream);
 int launch_bwd_tc(const st_layout& L, const BwdArgs& a, void* stream, bool* handled);
+// Device error word of the tensor-core kernels (1 after a bounded wait gave
+// up, -1 if it could not be read); clear resets it.
+int fwd_tc_device_error(bool clear);
+int bwd_tc_device_error(bool clear);
 int launch_merge(int D, int B, int H, int64_t S, int d, const float* part_out,
                  const float* part_lse, void* out, float* lse, int out_dtype, void* stream);
 int launch_bwd_preprocess(const BwdArgs& a, int64_t S, int dtype, void* stream);

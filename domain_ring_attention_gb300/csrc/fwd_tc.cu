@@ -1,13 +1,459 @@
-// Tensor-core (tcgen05 + TMA) forward: placeholder until the kernel lands.
-#include "common.h"
+// Forward sharded ring attention on tcgen05 tensor cores (sm_103a), bf16 in,
+// fp32 accumulation, bf16 out + fp32 lse.
+//
+// One CTA owns 256 query rows (two 128-row halves of one segment) of one
+// (batch, head) and walks the KV tiles in ring order: KV shard r, r-1, ...,
+// r+1 (mod D) for a query tile of shard r, the order in which rank r of a ring
+// receives its neighbours' K/V (ShardTensor summary, section 4, ring
+// attention).  On one GPU every shard is a row range of the same HBM buffer,
+// so "receiving" a shard is a TMA load of its next 128-key tile.  The running
+// (max, sum, O) state carried from tile to tile and shard to shard is the
+// log-sum-exp merge of the per-shard partials, done incrementally.
+//
+// Warp roles (384 threads):
+//   warp 0       TMA producer: Q once, then K and V tiles into a smem ring.
+//   warp 1       TMEM allocator and single-thread MMA issuer:
+//                  S_t = Q_t K^T    (tcgen05.mma, A and B from smem)
+//                  O_t += P_t V     (tcgen05.mma, A = P from TMEM, B from smem)
+//   warps 4-7    softmax for query half 0, warps 8-11 for half 1: read S_t from
+//                TMEM, mask (shard tails, causal / zigzag order), online
+//                softmax in the log2 domain, write P_t (bf16) back over S_t,
+//                rescale O_t when the running max grows by more than 2^8, and
+//                finally normalise O_t and store out / lse.
+// Tensor memory: S_0 | S_1 | O_0 | O_1 (128 + 128 + D + D of 512 columns).
+// Every barrier wait is bounded (see tc_ptx.cuh).
+#include <cuda.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "device.cuh"
+#include "tc_ptx.cuh"
 
 namespace st {
-int launch_fwd_tc(const st_layout&, const AttnArgs&, void*, bool* handled) {
-    *handled = false;
-    return 0;
+namespace {
+
+using namespace tc;
+
+constexpr int kM = 128;          // rows per query half (MMA M)
+constexpr int kNQ = 2;           // query halves per CTA
+constexpr int kN = 128;          // keys per KV tile
+constexpr int kThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;   // rescale O only when the max grows by > 2^8
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms per row
+    static constexpr int kChunkBytes = kM * 128;           // 128 rows x 64 bf16
+    static constexpr int kTileBytes = kChunks * kChunkBytes;
+    static constexpr int kStages = D == 64 ? 4 : 2;
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQOff + kNQ * kTileBytes;
+    static constexpr int kVOff = kKOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+    // q_full, k_full[S], v_full[S], kv_empty[S], s_full[NQ], p_full[NQ], o_done[NQ], drain
+    static constexpr int kNumBars = 2 + 3 * kStages + 3 * kNQ;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    static constexpr uint32_t kTmemCols = 512;
+    __host__ __device__ static constexpr uint32_t s_col(int t) { return (uint32_t)(t * kN); }
+    __host__ __device__ static constexpr uint32_t o_col(int t) { return (uint32_t)(kNQ * kN + t * D); }
+};
+
+struct FwdParams {
+    CUtensorMap tq;
+    CUtensorMap tk;
+    CUtensorMap tv;
+    SegTable tab;              // query tiles of kNQ * kM rows
+    __nv_bfloat16* out;
+    float* lse;
+    int B, H;
+    float scale_log2;          // softmax scale * log2(e)
+    int causal;
+};
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
 }
-int launch_bwd_tc(const st_layout&, const BwdArgs&, void*, bool* handled) {
-    *handled = false;
-    return 0;
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
 }
+
+// Kind of the (query half, KV tile) pair; an empty half skips everything.
+__device__ __forceinline__ int half_kind(int causal, int nat0, int nq, int natk, int nk) {
+    if (nq <= 0) return kSkip;
+    return classify(causal, nat0, nq, natk, nk, kN);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (sbase - raw);
+    const uint32_t sQ = sbase + C::kQOff, sK = sbase + C::kKOff, sV = sbase + C::kVOff;
+    const uint32_t bars = sbase + C::kBarOff;
+    const uint32_t bar_q = bars;
+    auto bar_k = [&](int s) { return bars + 8u * (1 + s); };
+    auto bar_v = [&](int s) { return bars + 8u * (1 + C::kStages + s); };
+    auto bar_e = [&](int s) { return bars + 8u * (1 + 2 * C::kStages + s); };
+    auto bar_s = [&](int t) { return bars + 8u * (1 + 3 * C::kStages + t); };
+    auto bar_p = [&](int t) { return bars + 8u * (1 + 3 * C::kStages + kNQ + t); };
+    auto bar_o = [&](int t) { return bars + 8u * (1 + 3 * C::kStages + 2 * kNQ + t); };
+    const uint32_t bar_drain = bars + 8u * (1 + 3 * C::kStages + 3 * kNQ);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = p.H;
+    const int b = blockIdx.y / H, h = blockIdx.y % H;
+    const QTile qt = locate_qtile(p.tab, blockIdx.x, kNQ * kM);
+    int nq_h[kNQ], nat_h[kNQ];
+#pragma unroll
+    for (int t = 0; t < kNQ; ++t) {
+        nq_h[t] = min(kM, max(0, qt.nq - kM * t));
+        nat_h[t] = qt.nat0 + kM * t;
+    }
+    const int causal = p.causal;
+    auto active = [&](int nk, int natk) {
+        bool any = false;
+#pragma unroll
+        for (int t = 0; t < kNQ; ++t) any |= half_kind(causal, nat_h[t], nq_h[t], natk, nk) != kSkip;
+        return any;
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar_k(s), 1);
+            mbar_init(bar_v(s), 1);
+            mbar_init(bar_e(s), 1);
+        }
+        for (int t = 0; t < kNQ; ++t) {
+            mbar_init(bar_s(t), 1);
+            mbar_init(bar_p(t), 128);
+            mbar_init(bar_o(t), 1);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&p.tq);
+        prefetch_tmap(&p.tk);
+        prefetch_tmap(&p.tv);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar_q, kNQ * C::kTileBytes);
+            for (int t = 0; t < kNQ; ++t)
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &p.tq, bar_q, c * 64, h,
+                                qt.row0 + kM * t, b);
+            int j = 0;
+            bool ok = true;
+            ring_walk<kN>(p.tab, qt.shard, [&](int, int kv0, int nk, int natk, bool) {
+                if (!ok || !active(nk, natk)) return;
+                const int s = j % C::kStages;
+                if (j >= C::kStages) ok = mbar_wait(bar_e(s), ((j / C::kStages) - 1) & 1, abort_flag);
+                if (!ok) return;
+                mbar_arrive_expect_tx(bar_k(s), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(sK + s * C::kTileBytes + c * C::kChunkBytes, &p.tk, bar_k(s), c * 64, h,
+                                kv0, b);
+                mbar_arrive_expect_tx(bar_v(s), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(sV + s * C::kTileBytes + c * C::kChunkBytes, &p.tv, bar_v(s), c * 64, h,
+                                kv0, b);
+                ++j;
+            });
+            // Let every load this thread issued land before the CTA can exit.
+            mbar_wait(bar_q, 0, abort_flag);
+            for (int jj = max(0, j - C::kStages); jj < j; ++jj) {
+                const int s = jj % C::kStages;
+                const uint32_t ph = (jj / C::kStages) & 1;
+                mbar_wait(bar_k(s), ph, abort_flag);
+                mbar_wait(bar_v(s), ph, abort_flag);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kN, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kM, D, 0, 1);
+            bool ok = mbar_wait(bar_q, 0, abort_flag);
+            tc_fence_after();
+            int j = 0;
+            ring_walk<kN>(p.tab, qt.shard, [&](int, int, int nk, int natk, bool) {
+                if (!ok || !active(nk, natk)) return;
+                const int s = j % C::kStages;
+                const uint32_t ph = (j / C::kStages) & 1;
+                ok = mbar_wait(bar_k(s), ph, abort_flag);
+                if (!ok) return;
+                tc_fence_after();
+                for (int t = 0; t < kNQ; ++t) {
+                    if (j > 0) {
+                        // P_t of the previous tile (aliasing S_t) must be consumed
+                        ok = mbar_wait(bar_o(t), (j - 1) & 1, abort_flag);
+                        if (!ok) return;
+                        tc_fence_after();
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                        const uint64_t a = smem_desc_sw128(sQ + t * C::kTileBytes + off, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(sK + s * C::kTileBytes + off, 16, 1024);
+                        mma_ss(tmem + C::s_col(t), a, bd, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar_s(t));
+                }
+                ok = mbar_wait(bar_v(s), ph, abort_flag);
+                if (!ok) return;
+                tc_fence_after();
+                for (int t = 0; t < kNQ; ++t) {
+                    ok = mbar_wait(bar_p(t), j & 1, abort_flag);
+                    if (!ok) return;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kN / 16; ++kk) {
+                        const uint64_t bd = smem_desc_sw128(sV + s * C::kTileBytes + kk * 2048,
+                                                            C::kChunkBytes, 1024);
+                        mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, bd, idesc_o,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar_o(t));
+                }
+                mma_commit(bar_e(s));
+                ++j;
+            });
+            // Every MMA issued above must finish before the TMEM is released.
+            mma_commit(bar_drain);
+            mbar_wait(bar_drain, 0, abort_flag);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ softmax + epilogue
+        const int t = (warp - 4) >> 2;
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const uint32_t tS = lane_base + C::s_col(t);
+        const uint32_t tO = lane_base + C::o_col(t);
+        const int nq = nq_h[t];
+        const int natq = nat_h[t] + row;
+        const float sl2 = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        int j = 0;
+        bool ok = true;
+        ring_walk<kN>(p.tab, qt.shard, [&](int, int, int nk, int natk, bool) {
+            if (!ok || !active(nk, natk)) return;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_s(t), j & 1, abort_flag));
+            if (!ok) return;
+            tc_fence_after();
+            const int kind = half_kind(causal, nat_h[t], nq, natk, nk);
+            bool resc = false;
+            float alpha = 1.f;
+            if (kind == kSkip) {
+                uint32_t z[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_st16(tS + c * 16, z);
+            } else {
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+                tmem_wait_ld();
+                if (kind == kPartial) {
+                    int limit = nk - 1;
+                    if (causal) limit = min(limit, natq - natk);
+#pragma unroll
+                    for (int c = 0; c < kN; ++c)
+                        if (c > limit) sr[c >> 5][c & 31] = 0xff800000u;   // -inf
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kN; c += 4) {
+                    mx0 = fmaxf(mx0, __uint_as_float(sr[c >> 5][c & 31]));
+                    mx1 = fmaxf(mx1, __uint_as_float(sr[c >> 5][(c + 1) & 31]));
+                    mx2 = fmaxf(mx2, __uint_as_float(sr[c >> 5][(c + 2) & 31]));
+                    mx3 = fmaxf(mx3, __uint_as_float(sr[c >> 5][(c + 3) & 31]));
+                }
+                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                float m_use = m;
+                if (m == -INFINITY) {
+                    m_use = mx;
+                } else if (mx - m > kRescaleLog2) {
+                    m_use = mx;
+                    resc = true;
+                    alpha = ex2(m - mx);
+                }
+                const float m_ref = m_use == -INFINITY ? 0.f : m_use;
+                float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * i]), sl2, -m_ref));
+                        const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), sl2, -m_ref));
+                        sum0 += p0;
+                        sum1 += p1;
+                        pk[i] = pack_bf16(p0, p1);
+                    }
+                    tmem_st16(tS + c * 16, pk);
+                }
+                l = l * alpha + (sum0 + sum1);
+                m = m_use;
+            }
+            if (__any_sync(0xffffffffu, resc) && j > 0) {
+                // O_t must hold every previous PV product before it is rescaled
+                ok = __all_sync(0xffffffffu, mbar_wait(bar_o(t), (j - 1) & 1, abort_flag));
+                if (ok) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(tO + c * 32, r);
+                    }
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar_p(t));
+            ++j;
+        });
+        if (ok && j > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_o(t), (j - 1) & 1, abort_flag));
+        if (ok) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int64_t grow = qt.row0 + kM * t + row;
+            __nv_bfloat16* dst = p.out + ((((int64_t)b * p.tab.S + grow) * H + h) * D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tO + c * 32, r);
+                tmem_wait_ld();
+                if (row < nq) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack_bf16(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+            if (row < nq)
+                p.lse[((int64_t)b * H + h) * p.tab.S + grow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// BSHD bf16 tensor as a 4-D map (d, H, S, B), box (64, 1, 128, 1), 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int d) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)S * H * d * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
+    using C = Cfg<D>;
+    FwdParams p;
+    const int S = (int)L.S;
+    if (!make_map(&p.tq, a.q, a.B, S, a.H, D) || !make_map(&p.tk, a.k, a.B, S, a.H, D) ||
+        !make_map(&p.tv, a.v, a.B, S, a.H, D))
+        return (int)cudaErrorInvalidValue;
+    fill_segtable(L, kNQ * kM, &p.tab);
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.lse = a.lse;
+    p.B = a.B;
+    p.H = a.H;
+    p.scale_log2 = a.scale * kLog2e;
+    p.causal = a.causal;
+    auto kern = fwd_tc_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return (int)e;
+    dim3 grid(p.tab.ntiles, a.B * a.H);
+    kern<<<grid, kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_fwd_tc(const st_layout& L, const AttnArgs& a, void* stream, bool* handled) {
+    *handled = true;
+    return a.d == 64 ? launch_t<64>(L, a, stream) : launch_t<128>(L, a, stream);
+}
+
+int fwd_tc_device_error(bool clear) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, tc::g_device_error, sizeof(int)) != cudaSuccess) return -1;
+    if (clear && v) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(tc::g_device_error, &zero, sizeof(int));
+    }
+    return v;
+}
+
 }  // namespace st

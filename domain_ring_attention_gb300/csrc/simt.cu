@@ -7,6 +7,7 @@
 // visited in ring order, each KV tile folded into a running (max, sum, O)
 // state -- the online form of the log-sum-exp merge of per-shard partials.
 #include <cfloat>
+#include <type_traits>
 #include <cmath>
 
 #include "device.cuh"
@@ -285,17 +286,23 @@ bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ Bw
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 const int c = tx + 16 * jj;
-                float s = 0.f, dp = 0.f;
+                // With fp32 inputs the score and dP dot products and the
+                // exponent are formed in double: each gradient element is a
+                // sum of P-weighted terms, and the fp32 rounding of a 64-term
+                // score (~1e-6 relative in P) alone approaches the 1e-5
+                // gradient bound.
+                using Acc = typename std::conditional<std::is_same<T, float>::value, double, float>::type;
+                Acc s = 0, dp = 0;
 #pragma unroll 8
                 for (int e = 0; e < D; ++e) {
-                    s = fmaf(Qs[r * LD + e], Ks[c * LD + e], s);
-                    dp = fmaf(dOs[r * LD + e], Vs[c * LD + e], dp);
+                    s += (Acc)Qs[r * LD + e] * (Acc)Ks[c * LD + e];
+                    dp += (Acc)dOs[r * LD + e] * (Acc)Vs[c * LD + e];
                 }
                 bool ok = r < qt.nq && c < kt.nq;
                 if (a.causal) ok = ok && (kt.nat0 + c <= qt.nat0 + r);
-                const float p = ok ? expf(s * scale - lse_s[r]) : 0.f;
-                Ps[r * LP + c] = p;
-                dSs[r * LP + c] = p * (dp - del_s[r]);
+                const Acc p = ok ? exp(s * (Acc)scale - (Acc)lse_s[r]) : (Acc)0;
+                Ps[r * LP + c] = (float)p;
+                dSs[r * LP + c] = (float)(p * (dp - (Acc)del_s[r]));
             }
         }
         __syncthreads();

@@ -150,6 +150,12 @@ int st_attn_bwd(const st_layout_t* layout, int B, int H, int d, int dtype, int c
 int st_permute(const st_layout_t* layout, int B, int H, int d, int dtype, int to_natural,
                const void* in, void* out, void* stream);
 
+/* Wait for `stream`, then report (and clear) the device error word of the
+ * tensor-core kernels: ST_ERR_DEVICE_TIMEOUT if one of their bounded
+ * barrier waits gave up since the last call (the kernel then stopped early
+ * and its outputs are not valid), else ST_OK.  Blocks the host. */
+int st_device_error(void* stream);
+
 /* Human-readable text for a status code (static storage). */
 const char* st_error_string(int code);
 
