@@ -1,10 +1,504 @@
-// Tensor-core backward: not yet available; the SIMT backward serves bf16.
-#include "common.h"
+// Backward sharded ring attention on tcgen05 tensor cores (sm_103a): bf16 in,
+// fp32 accumulation, dK / dV in the gradient dtype, dQ accumulated in fp32.
+//
+// KV-stationary: one CTA owns a 128-key tile of one (batch, head) -- its K and
+// V stay in shared memory and its dK, dV accumulate in tensor memory -- and
+// walks the 128-row query tiles that see it in ring order: the query shards
+// j, j+1, ..., j-1 (mod D) met by KV shard j as it travels around a ring
+// (ShardTensor summary, section 4, ring attention, training).  For each query
+// tile, with P = exp(scale S - lse) recomputed from the saved lse:
+//
+//   S^T  = K Q^T            (tcgen05.mma, smem x smem -> TMEM)
+//   dP^T = V dO^T           (tcgen05.mma, smem x smem -> TMEM)
+//   P^T, dS^T = P^T o (dP^T - Delta)   (softmax warps; P^T bf16 -> TMEM,
+//                                       dS^T bf16 -> swizzled smem)
+//   dV  += P^T dO           (A = P^T from TMEM)
+//   dK  += dS^T Q           (A = dS^T, K-major view of the smem tile)
+//   dQ_t = dS K             (A = dS, MN-major view of the same smem tile)
+//   dQ  += scale dQ_t       (reduction warps: TMEM -> red.global.add.v4.f32)
+//
+// Warp roles (384 threads): warp 0 TMA producer (+ lse / Delta staging),
+// warp 1 TMEM allocator + MMA issuer, warps 4-7 softmax (one key row per
+// thread) and the dK / dV epilogue, warps 8-11 dQ reduction (one query row
+// per thread).  Tensor memory: S^T|P^T, dP^T|dQ_t, dV, dK.  Every barrier
+// wait is bounded (tc_ptx.cuh).
+#include <cuda.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "device.cuh"
+#include "tc_ptx.cuh"
 
 namespace st {
-int launch_bwd_tc(const st_layout&, const BwdArgs&, void*, bool* handled) {
-    *handled = false;
-    return 0;
+namespace {
+
+using namespace tc;
+
+constexpr int kT = 128;          // keys per CTA, rows per query tile
+constexpr int kThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kChunkBytes = kT * 128;             // 128 rows x 64 bf16
+    static constexpr int kTileBytes = kChunks * kChunkBytes; // 128 rows x D bf16
+    static constexpr int kStages = D == 64 ? 2 : 1;
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kKOff + kTileBytes;
+    static constexpr int kQOff = kVOff + kTileBytes;               // [stage] Q tiles
+    static constexpr int kOOff = kQOff + kStages * kTileBytes;     // [stage] dO tiles
+    static constexpr int kSOff = kOOff + kStages * kTileBytes;     // dS^T, 128 x 128 bf16
+    static constexpr int kLOff = kSOff + 2 * kChunkBytes;          // [stage] lse*log2e, Delta
+    static constexpr int kBarOff = kLOff + kStages * 2 * kT * 4;
+    // kv_full, q_full[S], q_empty[S], s_full, ds_ready, it_done, dq_free, drain
+    static constexpr int kNumBars = 6 + 2 * kStages;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0;
+    static constexpr uint32_t kColDP = 128;
+    static constexpr uint32_t kColDV = 256;
+    static constexpr uint32_t kColDK = 256 + D;
+};
+
+struct BwdParams {
+    CUtensorMap tq;
+    CUtensorMap tk;
+    CUtensorMap tv;
+    CUtensorMap tdo;
+    SegTable tab;             // 128-row tiles
+    const float* lse;         // [B,H,S]
+    const float* delta;       // [B,H,S]
+    float* dq_acc;            // [B,S,H,D] fp32
+    void* dk;
+    void* dv;
+    int B, H;
+    float scale;
+    float scale_log2;
+    int causal;
+    int grad_f32;             // dK / dV written as fp32 (else bf16)
+};
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
 }
-int bwd_tc_device_error(bool) { return 0; }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// Walk the 128-row query tiles met by KV shard `j` in ring order: query shards
+// j, j+1, ..., j-1 (mod D); f(row0, nq, nat0).
+template <typename F>
+__device__ __forceinline__ void ring_walk_q(const SegTable& T, int j, F&& f) {
+    for (int t = 0; t < T.D; ++t) {
+        int r = j + t;
+        if (r >= T.D) r -= T.D;
+        for (int s = T.shard_seg[r]; s < T.shard_seg[r + 1]; ++s) {
+            const int b0 = T.seg_buf[s], b1 = T.seg_buf[s + 1], nat = T.seg_nat[s];
+            for (int q0 = b0; q0 < b1; q0 += kT) f(q0, min(kT, b1 - q0), nat + (q0 - b0));
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (sbase - raw);
+    const uint32_t sK = sbase + C::kKOff, sV = sbase + C::kVOff, sQ = sbase + C::kQOff,
+                   sO = sbase + C::kOOff, sS = sbase + C::kSOff;
+    float* lse_s = reinterpret_cast<float*>(gbase + C::kLOff);   // [stage][2][128]
+    const uint32_t bars = sbase + C::kBarOff;
+    const uint32_t bar_kv = bars;
+    auto bar_qf = [&](int s) { return bars + 8u * (1 + s); };
+    auto bar_qe = [&](int s) { return bars + 8u * (1 + C::kStages + s); };
+    const uint32_t bar_s = bars + 8u * (1 + 2 * C::kStages);
+    const uint32_t bar_ds = bar_s + 8;
+    const uint32_t bar_it = bar_s + 16;
+    const uint32_t bar_dqf = bar_s + 24;
+    const uint32_t bar_drain = bar_s + 32;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = p.H, S = p.tab.S;
+    const int b = blockIdx.y / H, h = blockIdx.y % H;
+    const QTile kt = locate_qtile(p.tab, blockIdx.x, kT);    // this CTA's key tile
+    const int causal = p.causal;
+    auto active = [&](int nq, int natq) {
+        return classify(causal, natq, nq, kt.nat0, kt.nq, kT) != kSkip;
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_kv, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar_qf(s), 33);
+            mbar_init(bar_qe(s), 1);
+        }
+        mbar_init(bar_s, 1);
+        mbar_init(bar_ds, 128);
+        mbar_init(bar_it, 1);
+        mbar_init(bar_dqf, 128);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int64_t lse_base = ((int64_t)b * H + h) * S;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer
+        uint32_t issued_tx = 0;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_4d(sK + c * C::kChunkBytes, &p.tk, bar_kv, c * 64, h, kt.row0, b);
+                tma_load_4d(sV + c * C::kChunkBytes, &p.tv, bar_kv, c * 64, h, kt.row0, b);
+            }
+        }
+        int i = 0;
+        bool ok = true;
+        ring_walk_q(p.tab, kt.shard, [&](int q0, int nq, int natq) {
+            if (!ok || !active(nq, natq)) return;
+            const int s = i % C::kStages;
+            if (i >= C::kStages)
+                ok = __all_sync(0xffffffffu, mbar_wait(bar_qe(s), ((i / C::kStages) - 1) & 1, abort_flag));
+            if (!ok) return;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar_qf(s), 2 * C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_4d(sQ + s * C::kTileBytes + c * C::kChunkBytes, &p.tq, bar_qf(s), c * 64, h, q0, b);
+                    tma_load_4d(sO + s * C::kTileBytes + c * C::kChunkBytes, &p.tdo, bar_qf(s), c * 64, h, q0, b);
+                }
+                issued_tx++;
+            }
+            float* ls = lse_s + s * 2 * kT;
+#pragma unroll
+            for (int e = 0; e < kT / 32; ++e) {
+                const int r = e * 32 + lane;
+                const bool valid = r < nq;
+                ls[r] = valid ? p.lse[lse_base + q0 + r] * kLog2e : INFINITY;
+                ls[kT + r] = valid ? p.delta[lse_base + q0 + r] : 0.f;
+            }
+            mbar_arrive(bar_qf(s));
+            ++i;
+        });
+        if (lane == 0) {
+            mbar_wait(bar_kv, 0, abort_flag);
+            for (int ii = max(0, i - C::kStages); ii < i; ++ii)
+                mbar_wait(bar_qf(ii % C::kStages), (ii / C::kStages) & 1, abort_flag);
+        }
+        (void)issued_tx;
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, 0, 0);      // S^T, dP^T
+            constexpr uint32_t id_kv = idesc_bf16_f32(kT, D, 0, 1);      // dV, dK (B MN-major)
+            constexpr uint32_t id_q = idesc_bf16_f32(kT, D, 1, 1);       // dQ (A and B MN-major)
+            bool ok = mbar_wait(bar_kv, 0, abort_flag);
+            tc_fence_after();
+            int i = 0;
+            ring_walk_q(p.tab, kt.shard, [&](int, int nq, int natq) {
+                if (!ok || !active(nq, natq)) return;
+                const int s = i % C::kStages;
+                ok = mbar_wait(bar_qf(s), (i / C::kStages) & 1, abort_flag);
+                if (ok && i > 0) ok = mbar_wait(bar_it, (i - 1) & 1, abort_flag);
+                if (ok && i > 0) ok = mbar_wait(bar_dqf, (i - 1) & 1, abort_flag);
+                if (!ok) return;
+                tc_fence_after();
+                const uint32_t q_t = sQ + s * C::kTileBytes, o_t = sO + s * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::kColS, smem_desc_sw128(sK + off, 16, 1024),
+                           smem_desc_sw128(q_t + off, 16, 1024), id_s, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::kColDP, smem_desc_sw128(sV + off, 16, 1024),
+                           smem_desc_sw128(o_t + off, 16, 1024), id_s, kk > 0);
+                }
+                mma_commit(bar_s);
+                ok = mbar_wait(bar_ds, i & 1, abort_flag);
+                if (!ok) return;
+                tc_fence_after();
+                // dV += P^T dO  (A: P^T bf16 in TMEM; B: dO, K = query rows, N = D)
+#pragma unroll
+                for (int kk = 0; kk < kT / 16; ++kk)
+                    mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
+                           smem_desc_sw128(o_t + kk * 2048, C::kChunkBytes, 1024), id_kv,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+                // dK += dS^T Q  (A: dS^T K-major in smem; B: Q, K = query rows, N = D)
+#pragma unroll
+                for (int kk = 0; kk < kT / 16; ++kk) {
+                    const uint32_t aoff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::kColDK, smem_desc_sw128(sS + aoff, 16, 1024),
+                           smem_desc_sw128(q_t + kk * 2048, C::kChunkBytes, 1024), id_kv,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                // dQ_t = dS K  (A: dS, M = query rows contiguous; B: K, K = keys, N = D)
+#pragma unroll
+                for (int kk = 0; kk < kT / 16; ++kk)
+                    mma_ss(tmem + C::kColDP, smem_desc_sw128(sS + kk * 2048, C::kChunkBytes, 1024),
+                           smem_desc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), id_q, kk > 0);
+                mma_commit(bar_it);
+                mma_commit(bar_qe(s));
+                ++i;
+            });
+            mma_commit(bar_drain);
+            mbar_wait(bar_drain, 0, abort_flag);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------ softmax (one key row per thread)
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;               // key row within the tile
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const int natk = kt.nat0 + r;
+        const float sl2 = p.scale_log2;
+        // dS^T row r: two 128-byte-swizzled 64-column chunks
+        const uint32_t ds_row = sS + (uint32_t)r * 128;
+        int i = 0;
+        bool ok = true;
+        ring_walk_q(p.tab, kt.shard, [&](int, int nq, int natq) {
+            if (!ok || !active(nq, natq)) return;
+            const int s = i % C::kStages;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_qf(s), (i / C::kStages) & 1, abort_flag));
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_s, i & 1, abort_flag));
+            if (!ok) return;
+            tc_fence_after();
+            const float* ls = lse_s + s * 2 * kT;
+            const int kind = classify(causal, natq, nq, kt.nat0, kt.nq, kT);
+            // query column c is visible to this key iff c < nq, r < nk and natk <= natq + c
+            const int cmin = (kind == kFull) ? 0 : (causal ? max(0, natk - natq) : 0);
+            const bool row_ok = r < kt.nq;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t sv[32], dv[32];
+                tmem_ld32(lane_base + C::kColS + c4 * 32, sv);
+                tmem_ld32(lane_base + C::kColDP + c4 * 32, dv);
+                tmem_wait_ld();
+                uint32_t pp[16], dd[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float pv[2], dsv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int c = c4 * 32 + 2 * e + u;
+                        const bool vis = row_ok && c >= cmin;   // c >= nq is killed by lse = +inf
+                        const float pr = vis ? ex2(fmaf(__uint_as_float(sv[2 * e + u]), sl2, -ls[c])) : 0.f;
+                        pv[u] = pr;
+                        dsv[u] = pr * (__uint_as_float(dv[2 * e + u]) - ls[kT + c]);
+                    }
+                    pp[e] = pack_bf16(pv[0], pv[1]);
+                    dd[e] = pack_bf16(dsv[0], dsv[1]);
+                }
+                tmem_st16(lane_base + C::kColS + c4 * 16, pp);
+                // dS^T columns c4*32 .. +31 = 16-byte units 4*(c4&1) .. +3 of chunk c4>>1
+                const uint32_t chunk = ds_row + (uint32_t)(c4 >> 1) * C::kChunkBytes;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t unit = (uint32_t)((c4 & 1) * 4 + u);
+                    st_shared_v4(chunk + ((unit ^ (uint32_t)(r & 7)) << 4), dd[4 * u], dd[4 * u + 1],
+                                 dd[4 * u + 2], dd[4 * u + 3]);
+                }
+            }
+            tmem_wait_st();
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(bar_ds);
+            ++i;
+        });
+        // epilogue: dV and scale * dK for this key row
+        if (ok && i > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_it, (i - 1) & 1, abort_flag));
+        if (ok) {
+            tc_fence_after();
+            const int64_t off = (((int64_t)b * S + kt.row0 + r) * H + h) * D;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+                const float mul = which == 0 ? 1.f : p.scale;
+                void* dst = which == 0 ? p.dv : p.dk;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    if (i > 0) {
+                        tmem_ld32(lane_base + col + c * 32, v);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = 0u;
+                    }
+                    if (r < kt.nq) {
+                        if (p.grad_f32) {
+                            float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(dst) + off + c * 32);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                d4[e] = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
+                                                    __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
+                        } else {
+                            uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + off + c * 32);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                d4[e] = make_uint4(
+                                    pack_bf16(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
+                                    pack_bf16(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
+                                    pack_bf16(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
+                                    pack_bf16(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
+                        }
+                    }
+                }
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------ dQ reduction (one query row per thread)
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const float sc = p.scale;
+        int i = 0;
+        bool ok = true;
+        ring_walk_q(p.tab, kt.shard, [&](int q0, int nq, int natq) {
+            if (!ok || !active(nq, natq)) return;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_it, i & 1, abort_flag));
+            if (!ok) return;
+            tc_fence_after();
+            float* dst = p.dq_acc + (((int64_t)b * S + q0 + r) * H + h) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(lane_base + C::kColDP + c * 32, v);
+                tmem_wait_ld();
+                if (r < nq) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        red_add_v4(dst + c * 32 + 4 * e, __uint_as_float(v[4 * e]) * sc,
+                                   __uint_as_float(v[4 * e + 1]) * sc, __uint_as_float(v[4 * e + 2]) * sc,
+                                   __uint_as_float(v[4 * e + 3]) * sc);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar_dqf);
+            ++i;
+        });
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int d) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)S * H * d * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+int launch_t(const st_layout& L, const BwdArgs& a, void* stream) {
+    using C = Cfg<D>;
+    BwdParams p;
+    const int S = (int)L.S;
+    if (!make_map(&p.tq, a.q, a.B, S, a.H, D) || !make_map(&p.tk, a.k, a.B, S, a.H, D) ||
+        !make_map(&p.tv, a.v, a.B, S, a.H, D) || !make_map(&p.tdo, a.dout, a.B, S, a.H, D))
+        return (int)cudaErrorInvalidValue;
+    fill_segtable(L, kT, &p.tab);
+    p.lse = a.lse;
+    p.delta = a.delta;
+    p.dq_acc = a.dq_acc;
+    p.dk = a.dk;
+    p.dv = a.dv;
+    p.B = a.B;
+    p.H = a.H;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * kLog2e;
+    p.causal = a.causal;
+    p.grad_f32 = a.grad_dtype == ST_DTYPE_F32 ? 1 : 0;
+    auto kern = bwd_tc_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return (int)e;
+    dim3 grid(p.tab.ntiles, a.B * a.H);
+    kern<<<grid, kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_bwd_tc(const st_layout& L, const BwdArgs& a, void* stream, bool* handled) {
+    *handled = true;
+    return a.d == 64 ? launch_t<64>(L, a, stream) : launch_t<128>(L, a, stream);
+}
+
+int bwd_tc_device_error(bool clear) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, tc::g_device_error, sizeof(int)) != cudaSuccess) return -1;
+    if (clear && v) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(tc::g_device_error, &zero, sizeof(int));
+    }
+    return v;
+}
+
 }  // namespace st

@@ -1,8 +1,8 @@
 // fp32 SIMT attention kernels (forward and backward).
 //
 // These carry the fp32 path, whose tolerance (max abs 1e-5 against the float64
-// definition) rules out tf32 tensor cores: every product and sum here is an
-// fp32 FFMA/FADD and every exponential is expf.  The structure is the same
+// definition) rules out tf32 tensor cores: the forward is fp32 FFMA/FADD with
+// expf; the backward forms its scores and gradient sums in double (see there).  The structure is the same
 // ring walk as the tensor-core path: one CTA per (query tile, b, h), KV shards
 // visited in ring order, each KV tile folded into a running (max, sum, O)
 // state -- the online form of the log-sum-exp merge of per-shard partials.
@@ -209,25 +209,34 @@ fwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ At
 
 // Backward, KV-stationary.  One CTA per (KV tile, b, h) accumulates dK and dV
 // for its keys over every query tile and adds its share of dQ into the fp32
-// workspace with atomics.  Thread (ty, tx) owns rows ty + 16 i and columns
+// accumulator with atomics.  Thread (ty, tx) owns rows ty + 16 i and columns
 // tx + 16 jj of each product (strided, so shared-memory reads do not conflict).
-template <int D>
-constexpr int bwd_smem_floats() {
-    return 4 * kBM * (D + 1) + 2 * kBM * (kBN + 1) + 2 * kBM;
+//
+// Acc is double for fp32 inputs: every gradient element is a long sum of
+// P-weighted terms that cancel (rows of dS sum to zero), and fp32 rounding of
+// the scores and of those sums alone comes close to the 1e-5 bound on
+// max|error| / RMS.  For bf16 inputs Acc is float.
+template <typename T>
+using BwdAcc = typename std::conditional<std::is_same<T, float>::value, double, float>::type;
+
+template <typename T, int D>
+constexpr size_t bwd_smem_bytes() {
+    return sizeof(float) * (4 * kBM * (D + 1) + 2 * kBM) + sizeof(BwdAcc<T>) * 2 * kBM * (kBN + 1);
 }
 
 template <typename T, typename TG, int D>
 __global__ void __launch_bounds__(kThreads)
 bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ BwdArgs a) {
+    using Acc = BwdAcc<T>;
     constexpr int LD = D + 1, LP = kBN + 1, NC = D / 16;
     extern __shared__ float4 smem4[];
-    float* Ks = reinterpret_cast<float*>(smem4);
+    Acc* Ps = reinterpret_cast<Acc*>(smem4);
+    Acc* dSs = Ps + kBM * LP;
+    float* Ks = reinterpret_cast<float*>(dSs + kBM * LP);
     float* Vs = Ks + kBN * LD;
     float* Qs = Vs + kBN * LD;
     float* dOs = Qs + kBM * LD;
-    float* Ps = dOs + kBM * LD;
-    float* dSs = Ps + kBM * LP;
-    float* lse_s = dSs + kBM * LP;
+    float* lse_s = dOs + kBM * LD;
     float* del_s = lse_s + kBM;
 
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
@@ -238,7 +247,7 @@ bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ Bw
     const T* k = static_cast<const T*>(a.k);
     const T* v = static_cast<const T*>(a.v);
     const T* dout = static_cast<const T*>(a.dout);
-    const float scale = a.scale;
+    const Acc scale = (Acc)a.scale;
 
     for (int e = tid; e < kBN * D; e += kThreads) {
         const int r = e / D, c = e % D;
@@ -251,11 +260,11 @@ bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ Bw
         Ks[r * LD + c] = kx;
         Vs[r * LD + c] = vx;
     }
-    float dK[4][NC], dV[4][NC];
+    Acc dK[4][NC], dV[4][NC];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int c = 0; c < NC; ++c) dK[i][c] = dV[i][c] = 0.f;
+        for (int c = 0; c < NC; ++c) dK[i][c] = dV[i][c] = 0;
 
     for (int qi = 0; qi < tab.ntiles; ++qi) {
         const QTile qt = locate_qtile(tab, qi, kBM);
@@ -286,12 +295,6 @@ bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ Bw
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 const int c = tx + 16 * jj;
-                // With fp32 inputs the score and dP dot products and the
-                // exponent are formed in double: each gradient element is a
-                // sum of P-weighted terms, and the fp32 rounding of a 64-term
-                // score (~1e-6 relative in P) alone approaches the 1e-5
-                // gradient bound.
-                using Acc = typename std::conditional<std::is_same<T, float>::value, double, float>::type;
                 Acc s = 0, dp = 0;
 #pragma unroll 8
                 for (int e = 0; e < D; ++e) {
@@ -300,16 +303,16 @@ bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ Bw
                 }
                 bool ok = r < qt.nq && c < kt.nq;
                 if (a.causal) ok = ok && (kt.nat0 + c <= qt.nat0 + r);
-                const Acc p = ok ? exp(s * (Acc)scale - (Acc)lse_s[r]) : (Acc)0;
-                Ps[r * LP + c] = (float)p;
-                dSs[r * LP + c] = (float)(p * (dp - (Acc)del_s[r]));
+                const Acc p = ok ? exp(s * scale - (Acc)lse_s[r]) : (Acc)0;
+                Ps[r * LP + c] = p;
+                dSs[r * LP + c] = p * (dp - (Acc)del_s[r]);
             }
         }
         __syncthreads();
         // dV += P^T dO ; dK += scale dS^T Q  (key rows ty + 16 i, columns tx + 16 jj)
 #pragma unroll 4
         for (int r = 0; r < kBM; ++r) {
-            float dov[NC], qv[NC];
+            Acc dov[NC], qv[NC];
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
                 dov[c] = dOs[r * LD + tx + 16 * c];
@@ -317,12 +320,12 @@ bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ Bw
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float p = Ps[r * LP + ty + 16 * i];
-                const float ds = dSs[r * LP + ty + 16 * i] * scale;
+                const Acc p = Ps[r * LP + ty + 16 * i];
+                const Acc ds = dSs[r * LP + ty + 16 * i] * scale;
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
-                    dV[i][c] = fmaf(p, dov[c], dV[i][c]);
-                    dK[i][c] = fmaf(ds, qv[c], dK[i][c]);
+                    dV[i][c] += p * dov[c];
+                    dK[i][c] += ds * qv[c];
                 }
             }
         }
@@ -330,18 +333,18 @@ bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ Bw
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = ty + 16 * i;
-            float acc[NC];
+            Acc acc[NC];
 #pragma unroll
-            for (int c = 0; c < NC; ++c) acc[c] = 0.f;
+            for (int c = 0; c < NC; ++c) acc[c] = 0;
             for (int n = 0; n < kBN; ++n) {
-                const float ds = dSs[r * LP + n];
+                const Acc ds = dSs[r * LP + n];
 #pragma unroll
-                for (int c = 0; c < NC; ++c) acc[c] = fmaf(ds, Ks[n * LD + tx + 16 * c], acc[c]);
+                for (int c = 0; c < NC; ++c) acc[c] += ds * (Acc)Ks[n * LD + tx + 16 * c];
             }
             if (r < qt.nq) {
                 float* dst = a.dq_acc + row_off(b, qt.row0 + r, h, S, H, D);
 #pragma unroll
-                for (int c = 0; c < NC; ++c) atomicAdd(dst + tx + 16 * c, acc[c] * scale);
+                for (int c = 0; c < NC; ++c) atomicAdd(dst + tx + 16 * c, (float)(acc[c] * scale));
             }
         }
     }
@@ -352,8 +355,8 @@ bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ Bw
         const int64_t o = row_off(b, kt.row0 + r, h, S, H, D);
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-            static_cast<TG*>(a.dk)[o + tx + 16 * c] = from_f32<TG>(dK[i][c]);
-            static_cast<TG*>(a.dv)[o + tx + 16 * c] = from_f32<TG>(dV[i][c]);
+            static_cast<TG*>(a.dk)[o + tx + 16 * c] = from_f32<TG>((float)dK[i][c]);
+            static_cast<TG*>(a.dv)[o + tx + 16 * c] = from_f32<TG>((float)dV[i][c]);
         }
     }
 }
@@ -371,7 +374,7 @@ int launch_fwd_simt_t(const SegTable& t, const AttnArgs& a, void* stream) {
 
 template <typename T, typename TG, int D>
 int launch_bwd_simt_t(const SegTable& t, const BwdArgs& a, void* stream) {
-    const size_t smem = sizeof(float) * bwd_smem_floats<D>();
+    const size_t smem = bwd_smem_bytes<T, D>();
     auto kern = bwd_simt_kernel<T, TG, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;

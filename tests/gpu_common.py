@@ -1,0 +1,78 @@
+"""Shared helpers for the GPU parity tests (CUDA library vs float64 oracle).
+
+Tolerances (stated for this method): fp32 inputs -- max abs error <= 1e-5;
+bf16 inputs with fp32 accumulation -- max abs <= 1e-2 and mean abs <= 1e-3.
+Gradients use the same bounds relative to the RMS of the oracle gradient.
+"""
+import numpy as np
+import torch
+
+import domain_ring_attention_gb300 as st
+from domain_ring_attention_gb300.workloads import make_inputs
+from oracle import attention as oa
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def assert_close(got, ref, dtype, name, rel_rms=False):
+    err = np.abs(np.asarray(got, dtype=np.float64) - ref)
+    den = float(np.sqrt(np.mean(ref * ref))) if rel_rms else 1.0
+    mx, mean = err.max() / den, err.mean() / den
+    if dtype == "f32":
+        assert mx <= 1e-5, "%s: max err %.3e > 1e-5" % (name, mx)
+    else:
+        assert mx <= 1e-2 and mean <= 1e-3, "%s: max %.3e mean %.3e" % (name, mx, mean)
+    return mx, mean
+
+
+def assert_lse(got, ref, dtype, name="lse"):
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin), name + ": -inf pattern differs"
+    assert_close(got[fin], ref[fin], dtype, name)
+
+
+def run_case(wl, seed=0, backward=True, grad_dtype=torch.float32):
+    q, k, v, do = (x.cuda() for x in make_inputs(wl, seed=seed, with_dout=True))
+    lay = st.Layout(wl.lens, wl.zigzag)
+    out, lse = st.st_attn_fwd(lay, q, k, v, causal=wl.causal)
+    res = {"out": out, "lse": lse, "in": (q, k, v, do)}
+    if backward:
+        res["grads"] = st.st_attn_bwd(lay, q, k, v, out, lse, do, causal=wl.causal,
+                                      grad_dtype=grad_dtype)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    return res
+
+
+def assert_no_device_error():
+    rc = st.load().st_device_error(None)
+    assert rc == 0, "device-side bounded wait gave up (%d)" % rc
+
+
+def check_rows(wl, res, rows, heads):
+    """Compare sampled rows of a large forward (rows are independent)."""
+    qd, kd, vd = res["in"][:3]
+    out, lse = f64(res["out"]), f64(res["lse"])
+    for (b, h) in heads:
+        qh = f64(qd[b:b + 1, :, h:h + 1])
+        kh = f64(kd[b:b + 1, :, h:h + 1])
+        vh = f64(vd[b:b + 1, :, h:h + 1])
+        ro, rl = oa.forward_rows(qh, kh, vh, wl.lens, wl.zigzag, wl.causal, rows, heads=[(0, 0)])
+        assert_close(out[b, rows, h], ro[(0, 0)], wl.dtype, "out[%d,%d]" % (b, h))
+        assert_close(lse[b, h, rows], rl[(0, 0)], wl.dtype, "lse[%d,%d]" % (b, h))
+
+
+def check_full(wl, res, backward=True):
+    """Element-by-element comparison of a whole (small) case with the oracle."""
+    q, k, v, do = (f64(x) for x in res["in"])
+    ro, rl = oa.forward(q, k, v, wl.lens, wl.zigzag, wl.causal)
+    assert_close(f64(res["out"]), ro, wl.dtype, "out")
+    assert_lse(f64(res["lse"]), rl, wl.dtype)
+    if backward:
+        rg = oa.backward(q, k, v, ro, rl, do, wl.lens, wl.zigzag, wl.causal)
+        for name, g, r in zip(("dq", "dk", "dv"), res["grads"], rg):
+            assert_close(f64(g), r, wl.dtype, name, rel_rms=True)
+
+
