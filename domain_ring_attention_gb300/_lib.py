@@ -37,7 +37,7 @@ PROTOTYPES = [
     ("st_layout_query", _I, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                              ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     ("st_attn_workspace_size", _I, [_P, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
-    ("st_attn_fwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    ("st_attn_fwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P, _SZ, _P]),
     ("st_attn_fwd_partials", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P]),
     ("st_attn_merge", _I, [_I, _I, _I, _I64, _I, _P, _P, _P, _P, _I, _P]),
     ("st_attn_bwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
@@ -167,21 +167,27 @@ def st_attn_workspace_size(layout, B, H, d, dtype, pass_):
     return int(n.value)
 
 
-def st_attn_fwd(layout, q, k, v, causal=False, scale=0.0, out=None, lse=None, stream=None):
-    """out, lse = attention of buffer-order BSHD q, k, v under ``layout``."""
+def st_attn_fwd(layout, q, k, v, causal=False, scale=0.0, out=None, lse=None, stream=None,
+                out_dtype=None):
+    """out, lse = attention of buffer-order BSHD q, k, v under ``layout``.
+
+    ``out_dtype`` defaults to the input dtype; torch.float32 returns the
+    normalised fp32 accumulator without the final rounding.
+    """
     B, S, H, d = _shape(q)
     for t, n in ((k, "k"), (v, "v")):
         _check_tensor(t, q.shape, q.dtype, n)
     _check_tensor(q, q.shape, q.dtype, "q")
+    odt = (out.dtype if out is not None else q.dtype) if out_dtype is None else out_dtype
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, device=q.device, dtype=odt)
     if lse is None:
         lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
-    _check_tensor(out, q.shape, q.dtype, "out")
+    _check_tensor(out, q.shape, odt, "out")
     _check_tensor(lse, (B, H, S), torch.float32, "lse")
     _check(load().st_attn_fwd(layout.handle, B, H, d, _dtype_code(q.dtype), int(bool(causal)),
-                              float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-                              None, 0, _stream(stream)), "st_attn_fwd")
+                              float(scale), _ptr(q), _ptr(k), _ptr(v), _dtype_code(odt), _ptr(out),
+                              _ptr(lse), None, 0, _stream(stream)), "st_attn_fwd")
     return out, lse
 
 

@@ -78,16 +78,17 @@ extern "C" int st_attn_workspace_size(const st_layout_t* L, int B, int H, int d,
 }
 
 extern "C" int st_attn_fwd(const st_layout_t* L, int B, int H, int d, int dtype, int causal,
-                           float scale, const void* q, const void* k, const void* v, void* out,
-                           float* lse, void* workspace, size_t ws_bytes, void* stream) {
+                           float scale, const void* q, const void* k, const void* v, int out_dtype,
+                           void* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
     (void)workspace;
     (void)ws_bytes;
     int rc = check_common(L, B, H, d, dtype, &scale);
     if (rc != ST_OK) return rc;
+    if (out_dtype != ST_DTYPE_F32 && out_dtype != dtype) return ST_ERR_UNSUPPORTED;
     if (!q || !k || !v || !out || !lse) return ST_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
         return ST_ERR_MISALIGNED;
-    st::AttnArgs a{q, k, v, out, lse, nullptr, nullptr, B, H, d, causal ? 1 : 0, scale};
+    st::AttnArgs a{q, k, v, out, lse, nullptr, nullptr, B, H, d, causal ? 1 : 0, scale, out_dtype};
     if (dtype == ST_DTYPE_BF16) {
         bool handled = false;
         rc = st::launch_fwd_tc(*L, a, stream, &handled);
@@ -108,7 +109,8 @@ extern "C" int st_attn_fwd_partials(const st_layout_t* L, int B, int H, int d, i
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(partial_out) ||
         !aligned16(partial_lse))
         return ST_ERR_MISALIGNED;
-    st::AttnArgs a{q, k, v, nullptr, nullptr, partial_out, partial_lse, B, H, d, causal ? 1 : 0, scale};
+    st::AttnArgs a{q, k, v, nullptr, nullptr, partial_out, partial_lse, B, H, d, causal ? 1 : 0, scale,
+                   ST_DTYPE_F32};
     st::SegTable t;
     st::fill_segtable(*L, 64, &t);
     return cuda_status(st::launch_fwd_simt(t, a, dtype, stream));

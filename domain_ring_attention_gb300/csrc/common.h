@@ -54,6 +54,7 @@ struct AttnArgs {
     int B, H, d;
     int causal;
     float scale;          // 1/sqrt(d) unless the caller chose another
+    int out_dtype;        // dtype of `out`
 };
 
 struct BwdArgs {

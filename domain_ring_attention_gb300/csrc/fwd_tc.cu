@@ -67,11 +67,12 @@ struct FwdParams {
     CUtensorMap tk;
     CUtensorMap tv;
     SegTable tab;              // query tiles of kNQ * kM rows
-    __nv_bfloat16* out;
+    void* out;                 // bf16, or fp32 when out_f32
     float* lse;
     int B, H;
     float scale_log2;          // softmax scale * log2(e)
     int causal;
+    int out_f32;
 };
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -352,20 +353,29 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int64_t grow = qt.row0 + kM * t + row;
-            __nv_bfloat16* dst = p.out + ((((int64_t)b * p.tab.S + grow) * H + h) * D);
+            const int64_t off = (((int64_t)b * p.tab.S + grow) * H + h) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tO + c * 32, r);
                 tmem_wait_ld();
                 if (row < nq) {
-                    uint32_t pk[16];
+                    if (p.out_f32) {
+                        float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off + c * 32);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pk[i] = pack_bf16(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+                        for (int i = 0; i < 8; ++i)
+                            d4[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                                __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+                    } else {
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+                        uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + off + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
                 }
             }
             if (row < nq)
@@ -425,7 +435,8 @@ int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
         !make_map(&p.tv, a.v, a.B, S, a.H, D))
         return (int)cudaErrorInvalidValue;
     fill_segtable(L, kNQ * kM, &p.tab);
-    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.out = a.out;
+    p.out_f32 = a.out_dtype == ST_DTYPE_F32 ? 1 : 0;
     p.lse = a.lse;
     p.B = a.B;
     p.H = a.H;

@@ -100,12 +100,14 @@ int st_attn_workspace_size(const st_layout_t* layout, int B, int H, int d, int d
  * own shard -- the order in which rank r receives K/V around a ring -- and
  * folds every KV tile into a running (max, sum, O) state, which is the
  * log-sum-exp merge of the per-shard partials carried out incrementally.
- *   q, k, v : [B,S,H,d] input dtype;  out : [B,S,H,d] input dtype;
- *   lse     : [B,H,S] fp32 (may not be NULL).
+ *   q, k, v   : [B,S,H,d] input dtype.
+ *   out_dtype : dtype of out: the input dtype, or ST_DTYPE_F32 (the fp32
+ *               accumulator normalised, without a final rounding to bf16).
+ *   out       : [B,S,H,d] out_dtype;  lse : [B,H,S] fp32 (may not be NULL).
  *   workspace, ws_bytes : unused by the forward (may be NULL / 0). */
 int st_attn_fwd(const st_layout_t* layout, int B, int H, int d, int dtype, int causal,
-                float scale, const void* q, const void* k, const void* v, void* out,
-                float* lse, void* workspace, size_t ws_bytes, void* stream);
+                float scale, const void* q, const void* k, const void* v, int out_dtype,
+                void* out, float* lse, void* workspace, size_t ws_bytes, void* stream);
 
 /* Forward that stops short of the merge: for every query row and every KV
  * shard j it writes the partial (O_j normalised by its own sum, lse_j) over

@@ -34,10 +34,22 @@ def assert_lse(got, ref, dtype, name="lse"):
 
 
 def run_case(wl, seed=0, backward=True, grad_dtype=torch.float32):
+    """Forward (and backward) of one workload.
+
+    For bf16 inputs the forward runs twice: with fp32 `out` (the value that is
+    held to the tolerance) and with bf16 `out` (what the backward consumes),
+    and the bf16 output must be the fp32 one rounded once.
+    """
     q, k, v, do = (x.cuda() for x in make_inputs(wl, seed=seed, with_dout=True))
     lay = st.Layout(wl.lens, wl.zigzag)
     out, lse = st.st_attn_fwd(lay, q, k, v, causal=wl.causal)
     res = {"out": out, "lse": lse, "in": (q, k, v, do)}
+    if q.dtype != torch.float32:
+        out32, lse32 = st.st_attn_fwd(lay, q, k, v, causal=wl.causal, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert torch.equal(out, out32.to(q.dtype)), "bf16 out is not the fp32 out rounded once"
+        assert torch.equal(lse, lse32)
+        res["out"], res["out_native"] = out32, out
     if backward:
         res["grads"] = st.st_attn_bwd(lay, q, k, v, out, lse, do, causal=wl.causal,
                                       grad_dtype=grad_dtype)

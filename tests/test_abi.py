@@ -87,13 +87,13 @@ def test_bad_calls_return_codes_without_a_gpu(lib):
     good = P(0x10000)
     lse = P(0x20000)
     fwd = lib.st_attn_fwd
-    assert fwd(None, 1, 1, 64, 1, 0, 0.0, good, good, good, good, lse, None, 0, None) == -1
-    assert fwd(lay.handle, 1, 1, 80, 1, 0, 0.0, good, good, good, good, lse, None, 0, None) == -3
-    assert fwd(lay.handle, 1, 1, 64, 5, 0, 0.0, good, good, good, good, lse, None, 0, None) == -3
-    assert fwd(lay.handle, 0, 1, 64, 1, 0, 0.0, good, good, good, good, lse, None, 0, None) == -8
-    assert fwd(lay.handle, 1, 1, 64, 1, 0, float("nan"), good, good, good, good, lse, None, 0, None) == -8
-    assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, None, good, good, good, lse, None, 0, None) == -1
-    assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, P(0x10008), good, good, good, lse, None, 0, None) == -4
+    assert fwd(None, 1, 1, 64, 1, 0, 0.0, good, good, good, 1, good, lse, None, 0, None) == -1
+    assert fwd(lay.handle, 1, 1, 80, 1, 0, 0.0, good, good, good, 1, good, lse, None, 0, None) == -3
+    assert fwd(lay.handle, 1, 1, 64, 5, 0, 0.0, good, good, good, 1, good, lse, None, 0, None) == -3
+    assert fwd(lay.handle, 0, 1, 64, 1, 0, 0.0, good, good, good, 1, good, lse, None, 0, None) == -8
+    assert fwd(lay.handle, 1, 1, 64, 1, 0, float("nan"), good, good, good, 1, good, lse, None, 0, None) == -8
+    assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, None, good, good, 1, good, lse, None, 0, None) == -1
+    assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, P(0x10008), good, good, 1, good, lse, None, 0, None) == -4
     bwd = lib.st_attn_bwd
     args = [good] * 6
     assert bwd(lay.handle, 1, 1, 64, 1, 0, 0.0, *args, 1, good, good, good, None, 0, None) == -5
