@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default="vit4096_s65536", choices=sorted(WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--heads", type=int, default=None,
+                   help="override H (a smaller capture of the same sequence shape for ncu)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     return p.parse_args()
@@ -207,6 +209,9 @@ def run_ours(args, rank, world):
     import domain_ring_attention_gb300 as st
     st.load()
     wl = WORKLOADS[args.workload]
+    if args.heads:
+        import dataclasses
+        wl = dataclasses.replace(wl, H=args.heads)
     dev = torch.device("cuda", torch.cuda.current_device())
     q_h, k_h, v_h = make_inputs(wl, seed=rank, device="cpu")
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)

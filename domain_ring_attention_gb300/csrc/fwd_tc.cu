@@ -25,7 +25,9 @@
 #include <cuda.h>
 
 #include <cmath>
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "device.cuh"
 #include "tc_ptx.cuh"
@@ -42,6 +44,7 @@ constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;   // rescale O only when the max grows by > 2^8
+constexpr int kMaxOrder = 4096;        // longest tile order passed as a kernel parameter
 
 template <int D>
 struct Cfg {
@@ -73,6 +76,8 @@ struct FwdParams {
     float scale_log2;          // softmax scale * log2(e)
     int causal;
     int out_f32;
+    int use_order;             // causal: CTAs take tiles heaviest first
+    uint16_t order[kMaxOrder];
 };
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -119,7 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = p.H;
     const int b = blockIdx.y / H, h = blockIdx.y % H;
-    const QTile qt = locate_qtile(p.tab, blockIdx.x, kNQ * kM);
+    const int tile = p.use_order ? (int)p.order[blockIdx.x] : (int)blockIdx.x;
+    const QTile qt = locate_qtile(p.tab, tile, kNQ * kM);
     int nq_h[kNQ], nat_h[kNQ];
 #pragma unroll
     for (int t = 0; t < kNQ; ++t) {
@@ -201,53 +207,70 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
+            // Issue order on the tensor pipe (ping-pong of the two halves):
+            //   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) ...
+            // so that while one softmax warpgroup works on S_t, the tensor core
+            // runs the other half's PV and next S.
             constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kM, D, 0, 1);
+            auto issue_s = [&](int t, int s) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::s_col(t), smem_desc_sw128(sQ + t * C::kTileBytes + off, 16, 1024),
+                           smem_desc_sw128(sK + s * C::kTileBytes + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar_s(t));
+            };
+            auto issue_pv = [&](int t, int s, int jj) {
+#pragma unroll
+                for (int kk = 0; kk < kN / 16; ++kk)
+                    mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
+                           smem_desc_sw128(sV + s * C::kTileBytes + kk * 2048, C::kChunkBytes, 1024),
+                           idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar_o(t));
+            };
             bool ok = mbar_wait(bar_q, 0, abort_flag);
             tc_fence_after();
             int j = 0;
             ring_walk<kN>(p.tab, qt.shard, [&](int, int, int nk, int natk, bool) {
                 if (!ok || !active(nk, natk)) return;
                 const int s = j % C::kStages;
-                const uint32_t ph = (j / C::kStages) & 1;
-                ok = mbar_wait(bar_k(s), ph, abort_flag);
+                ok = mbar_wait(bar_k(s), (j / C::kStages) & 1, abort_flag);
                 if (!ok) return;
                 tc_fence_after();
-                for (int t = 0; t < kNQ; ++t) {
-                    if (j > 0) {
-                        // P_t of the previous tile (aliasing S_t) must be consumed
-                        ok = mbar_wait(bar_o(t), (j - 1) & 1, abort_flag);
-                        if (!ok) return;
+                if (j == 0) {
+                    for (int t = 0; t < kNQ; ++t) issue_s(t, s);
+                } else {
+                    const int sp = (j - 1) % C::kStages;
+                    ok = mbar_wait(bar_v(sp), ((j - 1) / C::kStages) & 1, abort_flag);
+                    for (int t = 0; t < kNQ && ok; ++t) {
+                        ok = mbar_wait(bar_p(t), (j - 1) & 1, abort_flag);
+                        if (!ok) break;
                         tc_fence_after();
+                        issue_pv(t, sp, j - 1);
+                        // S_t(j) overwrites P_t(j-1): let PV_t(j-1) finish reading it
+                        ok = mbar_wait(bar_o(t), (j - 1) & 1, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(t, s);
                     }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                        const uint64_t a = smem_desc_sw128(sQ + t * C::kTileBytes + off, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(sK + s * C::kTileBytes + off, 16, 1024);
-                        mma_ss(tmem + C::s_col(t), a, bd, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar_s(t));
-                }
-                ok = mbar_wait(bar_v(s), ph, abort_flag);
-                if (!ok) return;
-                tc_fence_after();
-                for (int t = 0; t < kNQ; ++t) {
-                    ok = mbar_wait(bar_p(t), j & 1, abort_flag);
                     if (!ok) return;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < kN / 16; ++kk) {
-                        const uint64_t bd = smem_desc_sw128(sV + s * C::kTileBytes + kk * 2048,
-                                                            C::kChunkBytes, 1024);
-                        mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, bd, idesc_o,
-                               (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(bar_o(t));
+                    mma_commit(bar_e(sp));
                 }
-                mma_commit(bar_e(s));
                 ++j;
             });
+            if (ok && j > 0) {
+                const int sp = (j - 1) % C::kStages;
+                ok = mbar_wait(bar_v(sp), ((j - 1) / C::kStages) & 1, abort_flag);
+                for (int t = 0; t < kNQ && ok; ++t) {
+                    ok = mbar_wait(bar_p(t), (j - 1) & 1, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(t, sp, j - 1);
+                }
+                if (ok) mma_commit(bar_e(sp));
+            }
             // Every MMA issued above must finish before the TMEM is released.
             mma_commit(bar_drain);
             mbar_wait(bar_drain, 0, abort_flag);
@@ -292,15 +315,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     for (int c = 0; c < kN; ++c)
                         if (c > limit) sr[c >> 5][c & 31] = 0xff800000u;   // -inf
                 }
-                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+                float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < kN; c += 4) {
-                    mx0 = fmaxf(mx0, __uint_as_float(sr[c >> 5][c & 31]));
-                    mx1 = fmaxf(mx1, __uint_as_float(sr[c >> 5][(c + 1) & 31]));
-                    mx2 = fmaxf(mx2, __uint_as_float(sr[c >> 5][(c + 2) & 31]));
-                    mx3 = fmaxf(mx3, __uint_as_float(sr[c >> 5][(c + 3) & 31]));
+                    mx0 = max3(mx0, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c + 1) & 31]));
+                    mx1 = max3(mx1, __uint_as_float(sr[c >> 5][(c + 2) & 31]), __uint_as_float(sr[c >> 5][(c + 3) & 31]));
                 }
-                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                const float mx = fmaxf(mx0, mx1) * sl2;
                 float m_use = m;
                 if (m == -INFINITY) {
                     m_use = mx;
@@ -310,21 +331,33 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     alpha = ex2(m - mx);
                 }
                 const float m_ref = m_use == -INFINITY ? 0.f : m_use;
-                float sum0 = 0.f, sum1 = 0.f;
+                // p = 2^(s * scale * log2 e - m): one packed FMA per two scores,
+                // one MUFU ex2 per score, one packed add per two scores.
+                const uint64_t sl2x2 = f2_pack(sl2, sl2);
+                const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
+                uint64_t acc0 = 0, acc1 = 0;   // two packed partial sums (0.0f bits)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * i]), sl2, -m_ref));
-                        const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), sl2, -m_ref));
-                        sum0 += p0;
-                        sum1 += p1;
+                        const uint64_t x = ffma2(f2_pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
+                                                 sl2x2, negm2);
+                        float x0, x1;
+                        f2_unpack(x, x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        if (i & 1)
+                            acc1 = fadd2(acc1, f2_pack(p0, p1));
+                        else
+                            acc0 = fadd2(acc0, f2_pack(p0, p1));
                         pk[i] = pack_bf16(p0, p1);
                     }
                     tmem_st16(tS + c * 16, pk);
                 }
-                l = l * alpha + (sum0 + sum1);
+                float a0, a1, b0, b1;
+                f2_unpack(acc0, a0, a1);
+                f2_unpack(acc1, b0, b1);
+                l = l * alpha + ((a0 + a1) + (b0 + b1));
                 m = m_use;
             }
             if (__any_sync(0xffffffffu, resc) && j > 0) {
@@ -435,6 +468,26 @@ int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
         !make_map(&p.tv, a.v, a.B, S, a.H, D))
         return (int)cudaErrorInvalidValue;
     fill_segtable(L, kNQ * kM, &p.tab);
+    // Longest-processing-time-first order for causal work: a 256-row unit
+    // ending at natural position e sees about e keys.  Units of one head are
+    // issued heaviest first; heads stay in order (grid y) for L2 reuse of K/V.
+    p.use_order = 0;
+    if (a.causal && p.tab.ntiles <= kMaxOrder) {
+        std::vector<std::pair<int, int>> w;
+        w.reserve(p.tab.ntiles);
+        for (int s = 0; s < p.tab.nseg; ++s) {
+            const int len = p.tab.seg_buf[s + 1] - p.tab.seg_buf[s];
+            for (int tl = p.tab.seg_tile[s]; tl < p.tab.seg_tile[s + 1]; ++tl) {
+                const int local = (tl - p.tab.seg_tile[s]) * kNQ * kM;
+                const int nq = std::min(kNQ * kM, len - local);
+                w.emplace_back(-(p.tab.seg_nat[s] + local + nq), tl);
+            }
+        }
+        std::stable_sort(w.begin(), w.end(),
+                         [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first < y.first; });
+        for (int i = 0; i < p.tab.ntiles; ++i) p.order[i] = (uint16_t)w[i].second;
+        p.use_order = 1;
+    }
     p.out = a.out;
     p.out_f32 = a.out_dtype == ST_DTYPE_F32 ? 1 : 0;
     p.lse = a.lse;
