@@ -40,8 +40,8 @@ PROTOTYPES = [
     ("st_attn_fwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P, _SZ, _P]),
     ("st_attn_fwd_partials", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P]),
     ("st_attn_merge", _I, [_I, _I, _I, _I64, _I, _P, _P, _P, _P, _I, _P]),
-    ("st_attn_bwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
-                         _SZ, _P]),
+    ("st_attn_bwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P, _P, _I, _P, _P, _P,
+                         _P, _SZ, _P]),
     ("st_permute", _I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     ("st_error_string", ctypes.c_char_p, [_I]),
     ("st_last_cuda_error", _I, []),
@@ -220,10 +220,17 @@ def st_attn_merge(partial_out, partial_lse, out_dtype=torch.float32, out=None, l
 
 def st_attn_bwd(layout, q, k, v, out, lse, dout, causal=False, scale=0.0, grad_dtype=None,
                 workspace=None, stream=None):
-    """dq, dk, dv of sum(dout * out), in ``grad_dtype`` (default: fp32)."""
+    """dq, dk, dv of sum(dout * out), in ``grad_dtype`` (default: fp32).
+
+    ``out`` is the forward output in the input dtype or in fp32.
+    """
     B, S, H, d = _shape(q)
-    for t, n in ((k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+    for t, n in ((k, "k"), (v, "v"), (dout, "dout")):
         _check_tensor(t, q.shape, q.dtype, n)
+    if out.dtype != torch.float32:
+        _check_tensor(out, q.shape, q.dtype, "out")
+    else:
+        _check_tensor(out, q.shape, torch.float32, "out")
     _check_tensor(lse, (B, H, S), torch.float32, "lse")
     need = st_attn_workspace_size(layout, B, H, d, q.dtype, 1)
     if workspace is None:
@@ -231,9 +238,9 @@ def st_attn_bwd(layout, q, k, v, out, lse, dout, causal=False, scale=0.0, grad_d
     gdt = torch.float32 if grad_dtype is None else grad_dtype
     dq, dk, dv = (torch.empty(q.shape, device=q.device, dtype=gdt) for _ in range(3))
     _check(load().st_attn_bwd(layout.handle, B, H, d, _dtype_code(q.dtype), int(bool(causal)),
-                              float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-                              _ptr(dout), _dtype_code(gdt), _ptr(dq), _ptr(dk), _ptr(dv),
-                              _ptr(workspace),
+                              float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                              _dtype_code(out.dtype), _ptr(lse), _ptr(dout), _dtype_code(gdt),
+                              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream)),
            "st_attn_bwd")
     return dq, dk, dv

@@ -58,6 +58,28 @@ extern "C" int st_device_error(void* stream) {
     return (f || b) ? ST_ERR_DEVICE_TIMEOUT : ST_OK;
 }
 
+namespace st {
+
+BwdWorkspace bwd_workspace_layout(int64_t rows, int d, int dtype) {
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    BwdWorkspace w;
+    size_t off = 0;
+    w.dq_acc = off;
+    off += up((size_t)rows * d * sizeof(float));
+    w.delta = off;
+    off += up((size_t)rows * sizeof(float));
+    w.stats = off;
+    if (dtype == ST_DTYPE_F32) off += up(2 * (size_t)rows * sizeof(double));
+    w.h16 = off;
+    if (dtype == ST_DTYPE_BF16) off += 4 * up((size_t)rows * d * 2);
+    w.scales = off;
+    off += 256;
+    w.total = off;
+    return w;
+}
+
+}  // namespace st
+
 extern "C" int st_attn_workspace_size(const st_layout_t* L, int B, int H, int d, int dtype,
                                       int pass, size_t* bytes) {
     float scale = 1.f;
@@ -67,10 +89,7 @@ extern "C" int st_attn_workspace_size(const st_layout_t* L, int B, int H, int d,
     if (pass == 0) {
         *bytes = 0;
     } else if (pass == 1) {
-        const size_t rows = (size_t)B * (size_t)L->S * (size_t)H;
-        const size_t acc = rows * (size_t)d * sizeof(float);
-        // dq_acc then Delta, each 256-byte aligned
-        *bytes = ((acc + 255) & ~(size_t)255) + ((rows * sizeof(float) + 255) & ~(size_t)255);
+        *bytes = st::bwd_workspace_layout((int64_t)B * L->S * H, d, dtype).total;
     } else {
         return ST_ERR_INVALID_ARG;
     }
@@ -132,44 +151,70 @@ extern "C" int st_attn_merge(int D, int B, int H, int64_t S, int d, const float*
 
 extern "C" int st_attn_bwd(const st_layout_t* L, int B, int H, int d, int dtype, int causal,
                            float scale, const void* q, const void* k, const void* v,
-                           const void* out, const float* lse, const void* dout, int grad_dtype,
-                           void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
-                           void* stream) {
+                           const void* out, int out_dtype, const float* lse, const void* dout,
+                           int grad_dtype, void* dq, void* dk, void* dv, void* workspace,
+                           size_t ws_bytes, void* stream) {
     int rc = check_common(L, B, H, d, dtype, &scale);
     if (rc != ST_OK) return rc;
     if (grad_dtype != ST_DTYPE_F32 && grad_dtype != dtype) return ST_ERR_UNSUPPORTED;
+    if (out_dtype != ST_DTYPE_F32 && out_dtype != dtype) return ST_ERR_UNSUPPORTED;
     if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return ST_ERR_NULL;
     const void* ptrs[] = {q, k, v, out, lse, dout, dq, dk, dv};
     for (const void* p : ptrs)
         if (!aligned16(p)) return ST_ERR_MISALIGNED;
-    size_t need = 0;
-    rc = st_attn_workspace_size(L, B, H, d, dtype, 1, &need);
-    if (rc != ST_OK) return rc;
-    if (!workspace || ws_bytes < need) return ST_ERR_WORKSPACE;
+    const int64_t rows = (int64_t)B * L->S * H;
+    const st::BwdWorkspace w = st::bwd_workspace_layout(rows, d, dtype);
+    if (!workspace || ws_bytes < w.total) return ST_ERR_WORKSPACE;
     if (!aligned16(workspace)) return ST_ERR_MISALIGNED;
-    const size_t rows = (size_t)B * (size_t)L->S * (size_t)H;
-    const size_t acc_bytes = (rows * (size_t)d * sizeof(float) + 255) & ~(size_t)255;
+    char* ws = static_cast<char*>(workspace);
+    st::BwdArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.lse = lse;
+    a.dout = dout;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
     // fp32 gradients accumulate straight into dq; otherwise into the workspace
-    float* dq_acc = grad_dtype == ST_DTYPE_F32 ? static_cast<float*>(dq) : static_cast<float*>(workspace);
-    float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes);
-    st::BwdArgs a{q, k, v, out, lse, dout, dq, dk, dv, dq_acc, delta, B, H, d, causal ? 1 : 0,
-                  scale, grad_dtype};
+    a.dq_acc = grad_dtype == ST_DTYPE_F32 ? static_cast<float*>(dq) : reinterpret_cast<float*>(ws + w.dq_acc);
+    a.delta = reinterpret_cast<float*>(ws + w.delta);
+    a.B = B;
+    a.H = H;
+    a.d = d;
+    a.causal = causal ? 1 : 0;
+    a.scale = scale;
+    a.grad_dtype = grad_dtype;
+    a.out_dtype = out_dtype;
+    a.lse_d = reinterpret_cast<double*>(ws + w.stats);
+    a.delta_d = a.lse_d + rows;
+    const size_t plane = ((size_t)rows * d * 2 + 255) & ~(size_t)255;
+    for (int i = 0; i < 4; ++i) a.h16[i] = ws + w.h16 + i * plane;
+    a.amax_bits = reinterpret_cast<unsigned*>(ws + w.scales);
+    a.exps = reinterpret_cast<int*>(ws + w.scales + 64);
     cudaStream_t st_ = static_cast<cudaStream_t>(stream);
 
-    rc = cuda_status((int)cudaMemsetAsync(dq_acc, 0, rows * (size_t)d * sizeof(float), st_));
+    rc = cuda_status((int)cudaMemsetAsync(a.dq_acc, 0, (size_t)rows * d * sizeof(float), st_));
     if (rc != ST_OK) return rc;
-    rc = cuda_status(st::launch_bwd_preprocess(a, L->S, dtype, stream));
-    if (rc != ST_OK) return rc;
-    bool handled = false;
-    if (dtype == ST_DTYPE_BF16) {
-        rc = st::launch_bwd_tc(*L, a, stream, &handled);
-        if (handled && rc != 0) return cuda_status(rc);
-    }
-    if (!handled) {
+    if (dtype == ST_DTYPE_F32) {
         st::SegTable t;
         st::fill_segtable(*L, 64, &t);
+        rc = cuda_status(st::launch_rowstats_f64(t, a, stream));
+        if (rc != ST_OK) return rc;
         rc = cuda_status(st::launch_bwd_simt(t, a, dtype, stream));
         if (rc != ST_OK) return rc;
+    } else {
+        rc = cuda_status(st::launch_bwd_preprocess(a, L->S, dtype, stream));
+        if (rc != ST_OK) return rc;
+        rc = cuda_status((int)cudaMemsetAsync(a.amax_bits, 0, 64, st_));
+        if (rc != ST_OK) return rc;
+        rc = cuda_status(st::launch_fp16_copies(a, L->S, stream));
+        if (rc != ST_OK) return rc;
+        bool handled = false;
+        rc = cuda_status(st::launch_bwd_tc(*L, a, stream, &handled));
+        if (rc != ST_OK) return rc;
+        if (!handled) return ST_ERR_UNSUPPORTED;
     }
     if (grad_dtype == ST_DTYPE_F32) return ST_OK;
     return cuda_status(st::launch_dq_convert(a, L->S, grad_dtype, stream));

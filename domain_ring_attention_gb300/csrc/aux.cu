@@ -7,6 +7,8 @@
 // grid sized to a multiple of the SM count.
 #include <cmath>
 
+#include <cuda_fp16.h>
+
 #include "device.cuh"
 
 namespace st {
@@ -78,9 +80,9 @@ merge_kernel(int nparts, int B, int H, int S, const float* __restrict__ part_out
 }
 
 // Delta_i = sum_c dO_ic * O_ic in fp32 (backward preprocess).
-template <typename T, int D>
+template <typename TO, typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32)
-delta_kernel(int B, int H, int S, const T* __restrict__ o, const T* __restrict__ dout,
+delta_kernel(int B, int H, int S, const TO* __restrict__ o, const T* __restrict__ dout,
              float* __restrict__ delta) {
     constexpr int PER = D / 32;
     const int lane = threadIdx.x & 31;
@@ -163,21 +165,132 @@ int launch_bwd_preprocess(const BwdArgs& a, int64_t S, int dtype, void* stream) 
     const int64_t rows = (int64_t)a.B * S * a.H;
     const int grid = grid_for(rows);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    using bf16 = __nv_bfloat16;
     if (dtype == ST_DTYPE_F32) {
         auto o = static_cast<const float*>(a.out);
         auto g = static_cast<const float*>(a.dout);
         if (a.d == 64)
-            delta_kernel<float, 64><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
+            delta_kernel<float, float, 64><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
         else
-            delta_kernel<float, 128><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
-    } else {
-        auto o = static_cast<const __nv_bfloat16*>(a.out);
-        auto g = static_cast<const __nv_bfloat16*>(a.dout);
+            delta_kernel<float, float, 128><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
+    } else if (a.out_dtype == ST_DTYPE_F32) {
+        auto o = static_cast<const float*>(a.out);
+        auto g = static_cast<const bf16*>(a.dout);
         if (a.d == 64)
-            delta_kernel<__nv_bfloat16, 64><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
+            delta_kernel<float, bf16, 64><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
         else
-            delta_kernel<__nv_bfloat16, 128><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
+            delta_kernel<float, bf16, 128><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
+    } else {
+        auto o = static_cast<const bf16*>(a.out);
+        auto g = static_cast<const bf16*>(a.dout);
+        if (a.d == 64)
+            delta_kernel<bf16, bf16, 64><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
+        else
+            delta_kernel<bf16, bf16, 128><<<grid, kWarps * 32, 0, st>>>(a.B, a.H, (int)S, o, g, a.delta);
     }
+    return (int)cudaGetLastError();
+}
+
+namespace {
+
+// ---- exact fp16 operand copies for the tensor-core backward ----
+//
+// bf16 carries 8 significant bits and fp16 11, so a bf16 value times a power
+// of two is exactly representable in fp16 as long as it lands in fp16's normal
+// range.  Each tensor is scaled by 2^-e with e chosen from its max |x| so that
+// max |x| * 2^-e lies in [2^13, 2^14): nothing overflows and every value within
+// 2^-27 of the max stays normal.  The exponents (q, k, v, dO, and dS from the
+// bound |dS| <= 2 d max|dO| max|v|) go to the workspace for the backward kernel.
+
+__device__ __forceinline__ int norm_exp(float amax, int target) {
+    if (!(amax > 0.f) || !isfinite(amax)) return 0;
+    int E;
+    frexpf(amax, &E);            // amax = f * 2^E, f in [0.5, 1)
+    return E - 1 - target;       // amax * 2^-e in [2^target, 2^(target+1))
+}
+
+__global__ void __launch_bounds__(256)
+amax4_kernel(int64_t n8, const uint4* __restrict__ a, const uint4* __restrict__ b,
+             const uint4* __restrict__ c, const uint4* __restrict__ d, unsigned* __restrict__ amax_bits) {
+    const uint4* src[4] = {a, b, c, d};
+    float m[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const uint4 x = src[t][i];
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+                m[t] = fmaxf(m[t], fmaxf(fabsf(__bfloat162float(v2.x)), fabsf(__bfloat162float(v2.y))));
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        float v = m[t];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+        if ((threadIdx.x & 31) == 0) atomicMax(amax_bits + t, __float_as_uint(v));
+    }
+}
+
+__global__ void __launch_bounds__(256)
+fp16_copy_kernel(int64_t n8, int d, const uint4* __restrict__ a, const uint4* __restrict__ b,
+                 const uint4* __restrict__ c, const uint4* __restrict__ dd, uint4* __restrict__ oa,
+                 uint4* __restrict__ ob, uint4* __restrict__ oc, uint4* __restrict__ od,
+                 const unsigned* __restrict__ amax_bits, int* __restrict__ exps) {
+    const uint4* src[4] = {a, b, c, dd};
+    uint4* dst[4] = {oa, ob, oc, od};
+    float amax[4], mul[4];
+    int e[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        amax[t] = __uint_as_float(amax_bits[t]);
+        e[t] = norm_exp(amax[t], 13);
+        mul[t] = ldexpf(1.f, -e[t]);
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        for (int t = 0; t < 4; ++t) exps[t] = e[t];
+        exps[4] = norm_exp(2.f * (float)d * amax[3] * amax[2], 14);   // dS <= 2 d max|dO| max|v|
+    }
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const uint4 x = src[t][i];
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+            uint32_t r[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w[q]);
+                __half2 h2 = __floats2half2_rn(__bfloat162float(v2.x) * mul[t], __bfloat162float(v2.y) * mul[t]);
+                r[q] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            dst[t][i] = make_uint4(r[0], r[1], r[2], r[3]);
+        }
+    }
+}
+
+}  // namespace
+
+int launch_fp16_copies(const BwdArgs& a, int64_t S, void* stream) {
+    const int64_t n8 = (int64_t)a.B * S * a.H * a.d / 8;
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    const int64_t want = (n8 + 255) / 256;
+    const int grid = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto u4 = [](const void* p) { return static_cast<const uint4*>(p); };
+    amax4_kernel<<<grid, 256, 0, st>>>(n8, u4(a.q), u4(a.k), u4(a.v), u4(a.dout), a.amax_bits);
+    fp16_copy_kernel<<<grid, 256, 0, st>>>(n8, a.d, u4(a.q), u4(a.k), u4(a.v), u4(a.dout),
+                                           static_cast<uint4*>(a.h16[0]), static_cast<uint4*>(a.h16[1]),
+                                           static_cast<uint4*>(a.h16[2]), static_cast<uint4*>(a.h16[3]),
+                                           a.amax_bits, a.exps);
     return (int)cudaGetLastError();
 }
 

@@ -1,5 +1,6 @@
 // Backward sharded ring attention on tcgen05 tensor cores (sm_103a): bf16 in,
-// fp32 accumulation, dK / dV in the gradient dtype, dQ accumulated in fp32.
+// fp16 tensor-core operands (exact scaled copies, see BwdParams), fp32
+// accumulation, dK / dV in the gradient dtype, dQ accumulated in fp32.
 //
 // KV-stationary: one CTA owns a 128-key tile of one (batch, head) -- its K and
 // V stay in shared memory and its dK, dV accumulate in tensor memory -- and
@@ -10,8 +11,8 @@
 //
 //   S^T  = K Q^T            (tcgen05.mma, smem x smem -> TMEM)
 //   dP^T = V dO^T           (tcgen05.mma, smem x smem -> TMEM)
-//   P^T, dS^T = P^T o (dP^T - Delta)   (softmax warps; P^T bf16 -> TMEM,
-//                                       dS^T bf16 -> swizzled smem)
+//   P^T, dS^T = P^T o (dP^T - Delta)   (softmax warps; P^T fp16 -> TMEM,
+//                                       dS^T fp16 -> swizzled smem)
 //   dV  += P^T dO           (A = P^T from TMEM)
 //   dK  += dS^T Q           (A = dS^T, K-major view of the smem tile)
 //   dQ_t = dS K             (A = dS, MN-major view of the same smem tile)
@@ -23,6 +24,7 @@
 // per thread).  Tensor memory: S^T|P^T, dP^T|dQ_t, dV, dK.  Every barrier
 // wait is bounded (tc_ptx.cuh).
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include <cmath>
 #include <mutex>
@@ -42,14 +44,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int D>
 struct Cfg {
     static constexpr int kChunks = D / 64;
-    static constexpr int kChunkBytes = kT * 128;             // 128 rows x 64 bf16
-    static constexpr int kTileBytes = kChunks * kChunkBytes; // 128 rows x D bf16
+    static constexpr int kChunkBytes = kT * 128;             // 128 rows x 64 fp16
+    static constexpr int kTileBytes = kChunks * kChunkBytes; // 128 rows x D fp16
     static constexpr int kStages = D == 64 ? 2 : 1;
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kKOff + kTileBytes;
     static constexpr int kQOff = kVOff + kTileBytes;               // [stage] Q tiles
     static constexpr int kOOff = kQOff + kStages * kTileBytes;     // [stage] dO tiles
-    static constexpr int kSOff = kOOff + kStages * kTileBytes;     // dS^T, 128 x 128 bf16
+    static constexpr int kSOff = kOOff + kStages * kTileBytes;     // dS^T, 128 x 128 fp16
     static constexpr int kLOff = kSOff + 2 * kChunkBytes;          // [stage] lse*log2e, Delta
     static constexpr int kBarOff = kLOff + kStages * 2 * kT * 4;
     // kv_full, q_full[S], q_empty[S], s_full, ds_ready, it_done, dq_free, drain
@@ -63,6 +65,13 @@ struct Cfg {
     static constexpr uint32_t kColDK = 256 + D;
 };
 
+// Operands: exact fp16 copies of q, k, v, dO scaled by 2^-e (e per tensor,
+// chosen from its max |x|), so P and dS can be fed to the tensor cores in fp16
+// (11 significant bits) rather than bf16 (8): P enters as P * 2^14 and dS as
+// dS * 2^-e_dS, which keeps both inside fp16's normal range.  The scales are
+// undone in fp32 when S, dP and the gradients leave tensor memory.
+constexpr int kPShift = 14;
+
 struct BwdParams {
     CUtensorMap tq;
     CUtensorMap tk;
@@ -74,6 +83,7 @@ struct BwdParams {
     float* dq_acc;            // [B,S,H,D] fp32
     void* dk;
     void* dv;
+    const int* exps;          // scale exponents of q, k, v, dO, dS
     int B, H;
     float scale;
     float scale_log2;
@@ -94,6 +104,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// kind::f16 instruction descriptor with fp16 A and B (format 0) and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
@@ -208,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             for (int e = 0; e < kT / 32; ++e) {
                 const int r = e * 32 + lane;
                 const bool valid = r < nq;
-                ls[r] = valid ? p.lse[lse_base + q0 + r] * kLog2e : INFINITY;
+                ls[r] = valid ? p.lse[lse_base + q0 + r] * kLog2e - (float)kPShift : INFINITY;
                 ls[kT + r] = valid ? p.delta[lse_base + q0 + r] : 0.f;
             }
             mbar_arrive(bar_qf(s));
@@ -223,9 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, 0, 0);      // S^T, dP^T
-            constexpr uint32_t id_kv = idesc_bf16_f32(kT, D, 0, 1);      // dV, dK (B MN-major)
-            constexpr uint32_t id_q = idesc_bf16_f32(kT, D, 1, 1);       // dQ (A and B MN-major)
+            constexpr uint32_t id_s = idesc_f16_f32(kT, kT, 0, 0);      // S^T, dP^T
+            constexpr uint32_t id_kv = idesc_f16_f32(kT, D, 0, 1);      // dV, dK (B MN-major)
+            constexpr uint32_t id_q = idesc_f16_f32(kT, D, 1, 1);       // dQ (A and B MN-major)
             bool ok = mbar_wait(bar_kv, 0, abort_flag);
             tc_fence_after();
             int i = 0;
@@ -286,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const int r = quad * 32 + lane;               // key row within the tile
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         const int natk = kt.nat0 + r;
-        const float sl2 = p.scale_log2;
+        const float sl2 = ldexpf(p.scale_log2, p.exps[0] + p.exps[1]);    // S' -> scaled log2 units
+        const float dp_mul = ldexpf(1.f, p.exps[2] + p.exps[3]);           // dP' -> dP
+        const float ds_mul = ldexpf(1.f, -p.exps[4] - kPShift);            // P' (dP - Delta) -> dS'
         // dS^T row r: two 128-byte-swizzled 64-column chunks
         const uint32_t ds_row = sS + (uint32_t)r * 128;
         int i = 0;
@@ -319,10 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         const bool vis = row_ok && c >= cmin;   // c >= nq is killed by lse = +inf
                         const float pr = vis ? ex2(fmaf(__uint_as_float(sv[2 * e + u]), sl2, -ls[c])) : 0.f;
                         pv[u] = pr;
-                        dsv[u] = pr * (__uint_as_float(dv[2 * e + u]) - ls[kT + c]);
+                        dsv[u] = pr * fmaf(__uint_as_float(dv[2 * e + u]), dp_mul, -ls[kT + c]) * ds_mul;
                     }
-                    pp[e] = pack_bf16(pv[0], pv[1]);
-                    dd[e] = pack_bf16(dsv[0], dsv[1]);
+                    pp[e] = pack_f16(pv[0], pv[1]);
+                    dd[e] = pack_f16(dsv[0], dsv[1]);
                 }
                 tmem_st16(lane_base + C::kColS + c4 * 16, pp);
                 // dS^T columns c4*32 .. +31 = 16-byte units 4*(c4&1) .. +3 of chunk c4>>1
@@ -348,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
-                const float mul = which == 0 ? 1.f : p.scale;
+                const float mul = which == 0 ? ldexpf(1.f, p.exps[3] - kPShift)
+                                             : ldexpf(p.scale, p.exps[4] + p.exps[0]);
                 void* dst = which == 0 ? p.dv : p.dk;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -386,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        const float sc = p.scale;
+        const float sc = ldexpf(p.scale, p.exps[4] + p.exps[1]);
         int i = 0;
         bool ok = true;
         ring_walk_q(p.tab, kt.shard, [&](int q0, int nq, int natq) {
@@ -444,6 +468,7 @@ EncodeTiledFn get_encode() {
     return fn;
 }
 
+// BSHD fp16 tensor as a 4-D map (d, H, S, B), box (64, 1, 128, 1), 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int d) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return false;
@@ -451,7 +476,7 @@ bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int d) {
     const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)S * H * d * 2};
     const cuuint32_t box[4] = {64, 1, 128, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -461,8 +486,8 @@ int launch_t(const st_layout& L, const BwdArgs& a, void* stream) {
     using C = Cfg<D>;
     BwdParams p;
     const int S = (int)L.S;
-    if (!make_map(&p.tq, a.q, a.B, S, a.H, D) || !make_map(&p.tk, a.k, a.B, S, a.H, D) ||
-        !make_map(&p.tv, a.v, a.B, S, a.H, D) || !make_map(&p.tdo, a.dout, a.B, S, a.H, D))
+    if (!make_map(&p.tq, a.h16[0], a.B, S, a.H, D) || !make_map(&p.tk, a.h16[1], a.B, S, a.H, D) ||
+        !make_map(&p.tv, a.h16[2], a.B, S, a.H, D) || !make_map(&p.tdo, a.h16[3], a.B, S, a.H, D))
         return (int)cudaErrorInvalidValue;
     fill_segtable(L, kT, &p.tab);
     p.lse = a.lse;
@@ -470,6 +495,7 @@ int launch_t(const st_layout& L, const BwdArgs& a, void* stream) {
     p.dq_acc = a.dq_acc;
     p.dk = a.dk;
     p.dv = a.dv;
+    p.exps = a.exps;
     p.B = a.B;
     p.H = a.H;
     p.scale = a.scale;

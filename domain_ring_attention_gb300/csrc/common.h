@@ -73,7 +73,21 @@ struct BwdArgs {
     int causal;
     float scale;
     int grad_dtype;       // dtype of dq, dk, dv
+    int out_dtype;        // dtype of out
+    // fp32 inputs: row statistics recomputed in double
+    double* lse_d;        // [B,H,S]
+    double* delta_d;      // [B,H,S]
+    // bf16 inputs: exact fp16 copies of q, k, v, dO scaled by powers of two
+    void* h16[4];         // q, k, v, dO as fp16, [B,S,H,d]
+    unsigned* amax_bits;  // [4] max |x| of q, k, v, dO (float bits)
+    int* exps;            // [8] scale exponents: q, k, v, dO, dS
 };
+
+// Workspace layout of st_attn_bwd (each piece 256-byte aligned).
+struct BwdWorkspace {
+    size_t dq_acc, delta, stats, h16, scales, total;
+};
+BwdWorkspace bwd_workspace_layout(int64_t rows, int d, int dtype);
 
 // ---- launchers (return a cudaError_t value; 0 = success) ----
 int launch_fwd_simt(const SegTable& t, const AttnArgs& a, int dtype, void* stream);
@@ -87,6 +101,10 @@ int bwd_tc_device_error(bool clear);
 int launch_merge(int D, int B, int H, int64_t S, int d, const float* part_out,
                  const float* part_lse, void* out, float* lse, int out_dtype, void* stream);
 int launch_bwd_preprocess(const BwdArgs& a, int64_t S, int dtype, void* stream);
+// fp32 inputs: lse and Delta of every row recomputed in double
+int launch_rowstats_f64(const SegTable& t, const BwdArgs& a, void* stream);
+// bf16 inputs: max |x| and the scaled fp16 copies of q, k, v, dO
+int launch_fp16_copies(const BwdArgs& a, int64_t S, void* stream);
 int launch_dq_convert(const BwdArgs& a, int64_t S, int dtype, void* stream);
 int launch_permute(const SegTable& t, int B, int H, int d, int dtype, int to_natural,
                    const void* in, void* out, void* stream);

@@ -249,10 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(t, sp, j - 1);
-                        // S_t(j) overwrites P_t(j-1): let PV_t(j-1) finish reading it
-                        ok = mbar_wait(bar_o(t), (j - 1) & 1, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
+                        // S_t(j) overwrites P_t(j-1), which PV_t(j-1) reads: the
+                        // tcgen05.mma operations of one thread execute in issue
+                        // order, so S_t(j) can follow PV_t(j-1) without a wait.
                         issue_s(t, s);
                     }
                     if (!ok) return;
@@ -315,13 +314,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     for (int c = 0; c < kN; ++c)
                         if (c > limit) sr[c >> 5][c & 31] = 0xff800000u;   // -inf
                 }
-                float mx0 = -INFINITY, mx1 = -INFINITY;
+                // row max: four independent max3 chains of 16 steps each
+                float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < kN; c += 4) {
-                    mx0 = max3(mx0, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c + 1) & 31]));
-                    mx1 = max3(mx1, __uint_as_float(sr[c >> 5][(c + 2) & 31]), __uint_as_float(sr[c >> 5][(c + 3) & 31]));
+                for (int c = 0; c < kN; c += 8) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        mxa[u] = max3(mxa[u], __uint_as_float(sr[c >> 5][(c + 2 * u) & 31]),
+                                      __uint_as_float(sr[c >> 5][(c + 2 * u + 1) & 31]));
                 }
-                const float mx = fmaxf(mx0, mx1) * sl2;
+                const float mx = max3(mxa[0], mxa[1], fmaxf(mxa[2], mxa[3])) * sl2;
                 float m_use = m;
                 if (m == -INFINITY) {
                     m_use = mx;

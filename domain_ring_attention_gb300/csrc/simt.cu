@@ -221,7 +221,7 @@ using BwdAcc = typename std::conditional<std::is_same<T, float>::value, double, 
 
 template <typename T, int D>
 constexpr size_t bwd_smem_bytes() {
-    return sizeof(float) * (4 * kBM * (D + 1) + 2 * kBM) + sizeof(BwdAcc<T>) * 2 * kBM * (kBN + 1);
+    return sizeof(float) * 4 * kBM * (D + 1) + sizeof(BwdAcc<T>) * (2 * kBM * (kBN + 1) + 2 * kBM);
 }
 
 template <typename T, typename TG, int D>
@@ -232,12 +232,12 @@ bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ Bw
     extern __shared__ float4 smem4[];
     Acc* Ps = reinterpret_cast<Acc*>(smem4);
     Acc* dSs = Ps + kBM * LP;
-    float* Ks = reinterpret_cast<float*>(dSs + kBM * LP);
+    Acc* lse_s = dSs + kBM * LP;
+    Acc* del_s = lse_s + kBM;
+    float* Ks = reinterpret_cast<float*>(del_s + kBM);
     float* Vs = Ks + kBN * LD;
     float* Qs = Vs + kBN * LD;
     float* dOs = Qs + kBM * LD;
-    float* lse_s = dOs + kBM * LD;
-    float* del_s = lse_s + kBM;
 
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
     const int H = a.H, S = tab.S;
@@ -284,8 +284,13 @@ bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ Bw
         }
         if (tid < kBM) {
             const int64_t o = ((int64_t)b * H + h) * S + qt.row0 + tid;
-            lse_s[tid] = tid < qt.nq ? a.lse[o] : INFINITY;
-            del_s[tid] = tid < qt.nq ? a.delta[o] : 0.f;
+            if constexpr (std::is_same<Acc, double>::value) {
+                lse_s[tid] = tid < qt.nq ? a.lse_d[o] : (Acc)INFINITY;
+                del_s[tid] = tid < qt.nq ? a.delta_d[o] : (Acc)0;
+            } else {
+                lse_s[tid] = tid < qt.nq ? a.lse[o] : INFINITY;
+                del_s[tid] = tid < qt.nq ? a.delta[o] : 0.f;
+            }
         }
         __syncthreads();
         // P and dS for query rows ty + 16 i, key columns tx + 16 jj.
@@ -303,9 +308,9 @@ bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ Bw
                 }
                 bool ok = r < qt.nq && c < kt.nq;
                 if (a.causal) ok = ok && (kt.nat0 + c <= qt.nat0 + r);
-                const Acc p = ok ? exp(s * scale - (Acc)lse_s[r]) : (Acc)0;
+                const Acc p = ok ? exp(s * scale - lse_s[r]) : (Acc)0;
                 Ps[r * LP + c] = p;
-                dSs[r * LP + c] = p * (dp - (Acc)del_s[r]);
+                dSs[r * LP + c] = p * (dp - del_s[r]);
             }
         }
         __syncthreads();
@@ -361,6 +366,85 @@ bwd_simt_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ Bw
     }
 }
 
+// Row statistics of the fp32 backward in double: lse_i = log sum_j e^{s_ij}
+// and Delta_i = sum_j P_ij dP_ij over the visible keys of row i -- the same
+// Delta as rowsum(dO o out) with out = sum_j P_ij v_j, formed without the
+// rounding of the stored fp32 out and lse.  In rows with few visible keys
+// dP - Delta cancels heavily, and fp32 statistics alone would cost ~1e-5 of
+// the gradient's RMS.  One warp per row; lanes stride over the keys.
+template <int D>
+__global__ void __launch_bounds__(128)
+rowstats_f64_kernel(const __grid_constant__ SegTable tab, const __grid_constant__ BwdArgs a) {
+    __shared__ double qs[4][D];
+    __shared__ double gs[4][D];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = a.H, S = tab.S;
+    const int64_t rid = (int64_t)blockIdx.x * 4 + w;
+    if (rid >= (int64_t)a.B * H * S) return;
+    const int t = (int)(rid % S);
+    const int bh = (int)(rid / S);
+    const int b = bh / H, h = bh % H;
+    const float* q = static_cast<const float*>(a.q);
+    const float* k = static_cast<const float*>(a.k);
+    const float* v = static_cast<const float*>(a.v);
+    const float* g = static_cast<const float*>(a.dout);
+    for (int c = lane; c < D; c += 32) {
+        qs[w][c] = q[row_off(b, t, h, S, H, D) + c];
+        gs[w][c] = g[row_off(b, t, h, S, H, D) + c];
+    }
+    __syncwarp();
+    int st = 0;
+    while (st + 1 < tab.nseg && tab.seg_buf[st + 1] <= t) ++st;
+    const int pos_t = tab.seg_nat[st] + (t - tab.seg_buf[st]);
+    const double scale = (double)a.scale;
+    double m = -INFINITY, l = 0.0;
+    for (int s = 0; s < tab.nseg; ++s) {
+        for (int j = tab.seg_buf[s] + lane; j < tab.seg_buf[s + 1]; j += 32) {
+            if (a.causal && tab.seg_nat[s] + (j - tab.seg_buf[s]) > pos_t) continue;
+            const float* kr = k + row_off(b, j, h, S, H, D);
+            double dot = 0.0;
+            for (int c = 0; c < D; ++c) dot += qs[w][c] * (double)kr[c];
+            const double x = dot * scale;
+            if (x > m) {
+                l = l * exp(m - x) + 1.0;
+                m = x;
+            } else {
+                l += exp(x - m);
+            }
+        }
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+        const double m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const double l2 = __shfl_xor_sync(0xffffffffu, l, off);
+        const double mm = fmax(m, m2);
+        if (mm != -INFINITY) {
+            l = (m == -INFINITY ? 0.0 : l * exp(m - mm)) + (m2 == -INFINITY ? 0.0 : l2 * exp(m2 - mm));
+            m = mm;
+        }
+    }
+    const double lse = m + log(l);
+    double dl = 0.0;
+    for (int s = 0; s < tab.nseg; ++s) {
+        for (int j = tab.seg_buf[s] + lane; j < tab.seg_buf[s + 1]; j += 32) {
+            if (a.causal && tab.seg_nat[s] + (j - tab.seg_buf[s]) > pos_t) continue;
+            const float* kr = k + row_off(b, j, h, S, H, D);
+            const float* vr = v + row_off(b, j, h, S, H, D);
+            double dot = 0.0, dp = 0.0;
+            for (int c = 0; c < D; ++c) {
+                dot += qs[w][c] * (double)kr[c];
+                dp += gs[w][c] * (double)vr[c];
+            }
+            dl += exp(dot * scale - lse) * dp;
+        }
+    }
+    for (int off = 16; off > 0; off >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, off);
+    if (lane == 0) {
+        const int64_t o = ((int64_t)b * H + h) * S + t;
+        a.lse_d[o] = lse;
+        a.delta_d[o] = dl;
+    }
+}
+
 template <typename T, int D>
 int launch_fwd_simt_t(const SegTable& t, const AttnArgs& a, void* stream) {
     const size_t smem = sizeof(float) * fwd_smem_floats<D>();
@@ -393,16 +477,21 @@ int launch_fwd_simt(const SegTable& t, const AttnArgs& a, int dtype, void* strea
                      : launch_fwd_simt_t<__nv_bfloat16, 128>(t, a, stream);
 }
 
+int launch_rowstats_f64(const SegTable& t, const BwdArgs& a, void* stream) {
+    const int64_t rows = (int64_t)a.B * a.H * t.S;
+    const int grid = (int)((rows + 3) / 4);
+    if (a.d == 64)
+        rowstats_f64_kernel<64><<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(t, a);
+    else
+        rowstats_f64_kernel<128><<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(t, a);
+    return (int)cudaGetLastError();
+}
+
 int launch_bwd_simt(const SegTable& t, const BwdArgs& a, int dtype, void* stream) {
-    using bf16 = __nv_bfloat16;
-    if (dtype == ST_DTYPE_F32)
-        return a.d == 64 ? launch_bwd_simt_t<float, float, 64>(t, a, stream)
-                         : launch_bwd_simt_t<float, float, 128>(t, a, stream);
-    if (a.grad_dtype == ST_DTYPE_F32)
-        return a.d == 64 ? launch_bwd_simt_t<bf16, float, 64>(t, a, stream)
-                         : launch_bwd_simt_t<bf16, float, 128>(t, a, stream);
-    return a.d == 64 ? launch_bwd_simt_t<bf16, bf16, 64>(t, a, stream)
-                     : launch_bwd_simt_t<bf16, bf16, 128>(t, a, stream);
+    // fp32 inputs only: bf16 runs on the tensor-core backward
+    if (dtype != ST_DTYPE_F32) return (int)cudaErrorInvalidValue;
+    return a.d == 64 ? launch_bwd_simt_t<float, float, 64>(t, a, stream)
+                     : launch_bwd_simt_t<float, float, 128>(t, a, stream);
 }
 
 }  // namespace st

@@ -90,8 +90,10 @@ int st_layout_query(const st_layout_t* layout, int64_t* S, int64_t* offsets, int
                     int* D, int* zigzag);
 
 /* Workspace bytes needed by st_attn_fwd (pass = 0) or st_attn_bwd (pass = 1)
- * for these sizes.  The forward needs none (the merge is fused); the backward
- * needs an fp32 dQ accumulator [B,S,H,d] and the row sums Delta [B,H,S]. */
+ * for these sizes.  The forward needs none (the merge is fused).  The
+ * backward needs an fp32 dQ accumulator [B,S,H,d] and the row sums Delta
+ * [B,H,S]; bf16 adds four fp16 operand copies [B,S,H,d], fp32 adds the row
+ * statistics in double [2,B,H,S]. */
 int st_attn_workspace_size(const st_layout_t* layout, int B, int H, int d, int dtype,
                            int pass, size_t* bytes);
 
@@ -133,17 +135,25 @@ int st_attn_merge(int D, int B, int H, int64_t S, int d, const float* partial_ou
  * output gradient dout, writes dq, dk, dv ([B,S,H,d], all three in grad_dtype).
  * With P = exp(scale*QK^T - lse): dV = P^T dO; dP = dO V^T;
  * Delta = rowsum(dO * out); dS = P * (dP - Delta); dQ = scale dS K;
- * dK = scale dS^T Q.
- *   q, k, v, out, dout : input dtype;  lse : [B,H,S] fp32 from the forward.
+ * dK = scale dS^T Q.  The KV tiles of shard j meet the query shards in ring
+ * order j, j+1, ..., j-1 (mod D).
+ *   q, k, v, dout : input dtype;  lse : [B,H,S] fp32 from the forward.
+ *   out, out_dtype : the forward output, in the input dtype or ST_DTYPE_F32
+ *                (an fp32 out gives Delta without the bf16 rounding of out).
  *   grad_dtype : ST_DTYPE_F32 (fp32 gradients, no final rounding) or the
  *                input dtype.
  *   workspace  : at least st_attn_workspace_size(pass=1) bytes of device
  *                memory, 16-byte aligned; its contents on entry do not matter.
+ * bf16 inputs run on tcgen05 tensor cores with fp16 operands (exact copies
+ * of q, k, v, dO scaled by powers of two, made in the workspace) so that P
+ * and dS carry 11 significant bits; fp32 inputs run on the SIMT path with the
+ * row statistics (lse, Delta) recomputed in double.
  * Errors: as st_attn_fwd, plus ST_ERR_WORKSPACE. */
 int st_attn_bwd(const st_layout_t* layout, int B, int H, int d, int dtype, int causal,
                 float scale, const void* q, const void* k, const void* v,
-                const void* out, const float* lse, const void* dout, int grad_dtype,
-                void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream);
+                const void* out, int out_dtype, const float* lse, const void* dout,
+                int grad_dtype, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                void* stream);
 
 /* Reorder rows between buffer order and natural sequence order:
  *   to_natural = 1 : out[:, pos(t)] = in[:, t]   (buffer -> natural)

@@ -51,7 +51,8 @@ def run_case(wl, seed=0, backward=True, grad_dtype=torch.float32):
         assert torch.equal(lse, lse32)
         res["out"], res["out_native"] = out32, out
     if backward:
-        res["grads"] = st.st_attn_bwd(lay, q, k, v, out, lse, do, causal=wl.causal,
+        # the fp32 forward output gives Delta without the bf16 rounding of out
+        res["grads"] = st.st_attn_bwd(lay, q, k, v, res["out"], lse, do, causal=wl.causal,
                                       grad_dtype=grad_dtype)
     torch.cuda.synchronize()
     assert_no_device_error()

@@ -95,10 +95,11 @@ def test_bad_calls_return_codes_without_a_gpu(lib):
     assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, None, good, good, 1, good, lse, None, 0, None) == -1
     assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, P(0x10008), good, good, 1, good, lse, None, 0, None) == -4
     bwd = lib.st_attn_bwd
-    args = [good] * 6
-    assert bwd(lay.handle, 1, 1, 64, 1, 0, 0.0, *args, 1, good, good, good, None, 0, None) == -5
-    assert bwd(lay.handle, 1, 1, 64, 1, 0, 0.0, *args, 1, good, good, good, good, 16, None) == -5
-    assert bwd(lay.handle, 1, 1, 64, 0, 0, 0.0, *args, 1, good, good, good, good, 1 << 30, None) == -3
+    qkv = [good] * 3
+    assert bwd(lay.handle, 1, 1, 64, 1, 0, 0.0, *qkv, good, 1, lse, good, 1, good, good, good, None, 0, None) == -5
+    assert bwd(lay.handle, 1, 1, 64, 1, 0, 0.0, *qkv, good, 1, lse, good, 1, good, good, good, good, 16, None) == -5
+    assert bwd(lay.handle, 1, 1, 64, 0, 0, 0.0, *qkv, good, 0, lse, good, 1, good, good, good, good, 1 << 30, None) == -3
+    assert bwd(lay.handle, 1, 1, 64, 0, 0, 0.0, *qkv, good, 1, lse, good, 0, good, good, good, good, 1 << 30, None) == -3
     mrg = lib.st_attn_merge
     assert mrg(0, 1, 1, 64, 64, good, good, good, lse, 0, None) == -8
     assert mrg(33, 1, 1, 64, 64, good, good, good, lse, 0, None) == -8

@@ -2,6 +2,7 @@
 import pytest
 import torch
 
+import domain_ring_attention_gb300 as st
 from domain_ring_attention_gb300.workloads import WORKLOADS, Workload
 from gpu_common import assert_close, check_full, f64, run_case
 from oracle import attention as oa
@@ -43,6 +44,22 @@ def test_bf16_gradients_in_bf16():
         # the bf16 gradients are the fp32 ones rounded once (within one bf16 ulp,
         # since fp32 accumulation order may differ between runs)
         torch.testing.assert_close(g16.float(), g32, rtol=2.0 ** -7, atol=1e-6 * g32.abs().max().item())
+
+
+def test_backward_with_bf16_out():
+    """The backward also accepts the forward output in bf16 (Delta then carries
+    its rounding); on a non-causal case the gradients still meet the bound."""
+    wl = Workload("bf16out", B=1, H=2, d=64, lens=(384, 640), causal=False, zigzag=False, dtype="bf16")
+    res = run_case(wl, seed=21, backward=False)
+    q, k, v, do = res["in"]
+    lay = st.Layout(wl.lens)
+    grads = st.st_attn_bwd(lay, q, k, v, res["out_native"], res["lse"], do)
+    torch.cuda.synchronize()
+    Q, K, V, DO = (f64(x) for x in (q, k, v, do))
+    ro, rl = oa.forward(Q, K, V, wl.lens)
+    rg = oa.backward(Q, K, V, ro, rl, DO, wl.lens)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, rg):
+        assert_close(f64(g), r, "bf16", name, rel_rms=True)
 
 
 def test_vit1024_workload_backward_full():
