@@ -168,11 +168,13 @@ def st_attn_workspace_size(layout, B, H, d, dtype, pass_):
 
 
 def st_attn_fwd(layout, q, k, v, causal=False, scale=0.0, out=None, lse=None, stream=None,
-                out_dtype=None):
+                out_dtype=None, workspace=None):
     """out, lse = attention of buffer-order BSHD q, k, v under ``layout``.
 
     ``out_dtype`` defaults to the input dtype; torch.float32 returns the
-    normalised fp32 accumulator without the final rounding.
+    normalised fp32 accumulator without the final rounding.  ``workspace``
+    (uint8 device tensor of ``st_attn_workspace_size(..., 0)`` bytes) is
+    allocated here when not given.
     """
     B, S, H, d = _shape(q)
     for t, n in ((k, "k"), (v, "v")):
@@ -185,9 +187,13 @@ def st_attn_fwd(layout, q, k, v, causal=False, scale=0.0, out=None, lse=None, st
         lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
     _check_tensor(out, q.shape, odt, "out")
     _check_tensor(lse, (B, H, S), torch.float32, "lse")
+    if workspace is None:
+        need = st_attn_workspace_size(layout, B, H, d, q.dtype, 0)
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
     _check(load().st_attn_fwd(layout.handle, B, H, d, _dtype_code(q.dtype), int(bool(causal)),
                               float(scale), _ptr(q), _ptr(k), _ptr(v), _dtype_code(odt), _ptr(out),
-                              _ptr(lse), None, 0, _stream(stream)), "st_attn_fwd")
+                              _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "st_attn_fwd")
     return out, lse
 
 

@@ -78,6 +78,11 @@ BwdWorkspace bwd_workspace_layout(int64_t rows, int d, int dtype) {
     return w;
 }
 
+size_t fwd_workspace_bytes(int64_t rows, int d, int dtype) {
+    if (dtype != ST_DTYPE_BF16) return 0;
+    return (((size_t)rows * d * 2 + 255) & ~(size_t)255) + 256;
+}
+
 }  // namespace st
 
 extern "C" int st_attn_workspace_size(const st_layout_t* L, int B, int H, int d, int dtype,
@@ -87,7 +92,7 @@ extern "C" int st_attn_workspace_size(const st_layout_t* L, int B, int H, int d,
     const int rc = check_common(L, B, H, d, dtype, &scale);
     if (rc != ST_OK) return rc;
     if (pass == 0) {
-        *bytes = 0;
+        *bytes = st::fwd_workspace_bytes((int64_t)B * L->S * H, d, dtype);
     } else if (pass == 1) {
         *bytes = st::bwd_workspace_layout((int64_t)B * L->S * H, d, dtype).total;
     } else {
@@ -99,19 +104,29 @@ extern "C" int st_attn_workspace_size(const st_layout_t* L, int B, int H, int d,
 extern "C" int st_attn_fwd(const st_layout_t* L, int B, int H, int d, int dtype, int causal,
                            float scale, const void* q, const void* k, const void* v, int out_dtype,
                            void* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
-    (void)workspace;
-    (void)ws_bytes;
     int rc = check_common(L, B, H, d, dtype, &scale);
     if (rc != ST_OK) return rc;
     if (out_dtype != ST_DTYPE_F32 && out_dtype != dtype) return ST_ERR_UNSUPPORTED;
     if (!q || !k || !v || !out || !lse) return ST_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
         return ST_ERR_MISALIGNED;
-    st::AttnArgs a{q, k, v, out, lse, nullptr, nullptr, B, H, d, causal ? 1 : 0, scale, out_dtype};
+    st::AttnArgs a{q, k, v, out, lse, nullptr, nullptr, B, H, d, causal ? 1 : 0, scale, out_dtype,
+                   nullptr, nullptr, nullptr};
     if (dtype == ST_DTYPE_BF16) {
+        const int64_t rows = (int64_t)B * L->S * H;
+        const size_t need = st::fwd_workspace_bytes(rows, d, dtype);
+        if (!workspace || ws_bytes < need) return ST_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return ST_ERR_MISALIGNED;
+        char* ws = static_cast<char*>(workspace);
+        a.v16 = ws;
+        a.amax_bits = reinterpret_cast<unsigned*>(ws + need - 256);
+        a.exps = reinterpret_cast<int*>(ws + need - 128);
+        rc = cuda_status(st::launch_fp16_copy1(v, a.v16, rows * d, a.amax_bits, a.exps, stream));
+        if (rc != ST_OK) return rc;
         bool handled = false;
         rc = st::launch_fwd_tc(*L, a, stream, &handled);
         if (handled) return cuda_status(rc);
+        return ST_ERR_UNSUPPORTED;
     }
     st::SegTable t;
     st::fill_segtable(*L, 64, &t);

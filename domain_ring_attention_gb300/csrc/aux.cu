@@ -209,15 +209,22 @@ __device__ __forceinline__ int norm_exp(float amax, int target) {
     return E - 1 - target;       // amax * 2^-e in [2^target, 2^(target+1))
 }
 
+struct Fp16Job {
+    const uint4* src[4];
+    uint4* dst[4];
+};
+
+// max |x| of NT bf16 tensors of n8 * 8 elements each (float bits, atomicMax)
+template <int NT>
 __global__ void __launch_bounds__(256)
-amax4_kernel(int64_t n8, const uint4* __restrict__ a, const uint4* __restrict__ b,
-             const uint4* __restrict__ c, const uint4* __restrict__ d, unsigned* __restrict__ amax_bits) {
-    const uint4* src[4] = {a, b, c, d};
-    float m[4] = {0.f, 0.f, 0.f, 0.f};
+amax_kernel(int64_t n8, const __grid_constant__ Fp16Job job, unsigned* __restrict__ amax_bits) {
+    float m[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) m[t] = 0.f;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const uint4 x = src[t][i];
+        for (int t = 0; t < NT; ++t) {
+            const uint4 x = job.src[t][i];
             const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -227,7 +234,7 @@ amax4_kernel(int64_t n8, const uint4* __restrict__ a, const uint4* __restrict__ 
         }
     }
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
+    for (int t = 0; t < NT; ++t) {
         float v = m[t];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
@@ -235,29 +242,29 @@ amax4_kernel(int64_t n8, const uint4* __restrict__ a, const uint4* __restrict__ 
     }
 }
 
+// fp16 copies dst[t] = src[t] * 2^-e_t, exact; the exponents go to exps[0..NT).
+// With ds_d > 0 (the backward: q, k, v, dO) exps[4] gets the dS exponent from
+// the bound |dS| <= 2 d max|dO| max|v|.
+template <int NT>
 __global__ void __launch_bounds__(256)
-fp16_copy_kernel(int64_t n8, int d, const uint4* __restrict__ a, const uint4* __restrict__ b,
-                 const uint4* __restrict__ c, const uint4* __restrict__ dd, uint4* __restrict__ oa,
-                 uint4* __restrict__ ob, uint4* __restrict__ oc, uint4* __restrict__ od,
+fp16_copy_kernel(int64_t n8, int ds_d, const __grid_constant__ Fp16Job job,
                  const unsigned* __restrict__ amax_bits, int* __restrict__ exps) {
-    const uint4* src[4] = {a, b, c, dd};
-    uint4* dst[4] = {oa, ob, oc, od};
-    float amax[4], mul[4];
-    int e[4];
+    float amax[NT], mul[NT];
+    int e[NT];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
+    for (int t = 0; t < NT; ++t) {
         amax[t] = __uint_as_float(amax_bits[t]);
         e[t] = norm_exp(amax[t], 13);
         mul[t] = ldexpf(1.f, -e[t]);
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) {
-        for (int t = 0; t < 4; ++t) exps[t] = e[t];
-        exps[4] = norm_exp(2.f * (float)d * amax[3] * amax[2], 14);   // dS <= 2 d max|dO| max|v|
+        for (int t = 0; t < NT; ++t) exps[t] = e[t];
+        if (NT == 4 && ds_d > 0) exps[4] = norm_exp(2.f * (float)ds_d * amax[NT - 1] * amax[NT > 2 ? 2 : 0], 14);
     }
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const uint4 x = src[t][i];
+        for (int t = 0; t < NT; ++t) {
+            const uint4 x = job.src[t][i];
             const uint32_t w[4] = {x.x, x.y, x.z, x.w};
             uint32_t r[4];
 #pragma unroll
@@ -266,15 +273,12 @@ fp16_copy_kernel(int64_t n8, int d, const uint4* __restrict__ a, const uint4* __
                 __half2 h2 = __floats2half2_rn(__bfloat162float(v2.x) * mul[t], __bfloat162float(v2.y) * mul[t]);
                 r[q] = *reinterpret_cast<uint32_t*>(&h2);
             }
-            dst[t][i] = make_uint4(r[0], r[1], r[2], r[3]);
+            job.dst[t][i] = make_uint4(r[0], r[1], r[2], r[3]);
         }
     }
 }
 
-}  // namespace
-
-int launch_fp16_copies(const BwdArgs& a, int64_t S, void* stream) {
-    const int64_t n8 = (int64_t)a.B * S * a.H * a.d / 8;
+int fp16_grid(int64_t n8) {
     static int sms = 0;
     if (sms == 0) {
         int dev = 0;
@@ -283,14 +287,38 @@ int launch_fp16_copies(const BwdArgs& a, int64_t S, void* stream) {
         if (sms <= 0) sms = 1;
     }
     const int64_t want = (n8 + 255) / 256;
-    const int grid = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
+    return (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
+}
+
+}  // namespace
+
+int launch_fp16_copies(const BwdArgs& a, int64_t S, void* stream) {
+    const int64_t n8 = (int64_t)a.B * S * a.H * a.d / 8;
+    Fp16Job job;
+    const void* src[4] = {a.q, a.k, a.v, a.dout};
+    for (int t = 0; t < 4; ++t) {
+        job.src[t] = static_cast<const uint4*>(src[t]);
+        job.dst[t] = static_cast<uint4*>(a.h16[t]);
+    }
+    const int grid = fp16_grid(n8);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    auto u4 = [](const void* p) { return static_cast<const uint4*>(p); };
-    amax4_kernel<<<grid, 256, 0, st>>>(n8, u4(a.q), u4(a.k), u4(a.v), u4(a.dout), a.amax_bits);
-    fp16_copy_kernel<<<grid, 256, 0, st>>>(n8, a.d, u4(a.q), u4(a.k), u4(a.v), u4(a.dout),
-                                           static_cast<uint4*>(a.h16[0]), static_cast<uint4*>(a.h16[1]),
-                                           static_cast<uint4*>(a.h16[2]), static_cast<uint4*>(a.h16[3]),
-                                           a.amax_bits, a.exps);
+    amax_kernel<4><<<grid, 256, 0, st>>>(n8, job, a.amax_bits);
+    fp16_copy_kernel<4><<<grid, 256, 0, st>>>(n8, a.d, job, a.amax_bits, a.exps);
+    return (int)cudaGetLastError();
+}
+
+int launch_fp16_copy1(const void* src, void* dst, int64_t elems, unsigned* amax_bits, int* exps,
+                      void* stream) {
+    const int64_t n8 = elems / 8;
+    Fp16Job job{};
+    job.src[0] = static_cast<const uint4*>(src);
+    job.dst[0] = static_cast<uint4*>(dst);
+    const int grid = fp16_grid(n8);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(amax_bits, 0, sizeof(unsigned), st);
+    if (e != cudaSuccess) return (int)e;
+    amax_kernel<1><<<grid, 256, 0, st>>>(n8, job, amax_bits);
+    fp16_copy_kernel<1><<<grid, 256, 0, st>>>(n8, 0, job, amax_bits, exps);
     return (int)cudaGetLastError();
 }
 

@@ -55,7 +55,14 @@ struct AttnArgs {
     int causal;
     float scale;          // 1/sqrt(d) unless the caller chose another
     int out_dtype;        // dtype of `out`
+    // bf16 forward: exact fp16 copy of v scaled by 2^-exps[0] (workspace)
+    void* v16;
+    unsigned* amax_bits;
+    int* exps;
 };
+
+// Workspace of st_attn_fwd: bf16 needs the fp16 copy of v plus 256 bytes.
+size_t fwd_workspace_bytes(int64_t rows, int d, int dtype);
 
 struct BwdArgs {
     const void* q;
@@ -105,6 +112,9 @@ int launch_bwd_preprocess(const BwdArgs& a, int64_t S, int dtype, void* stream);
 int launch_rowstats_f64(const SegTable& t, const BwdArgs& a, void* stream);
 // bf16 inputs: max |x| and the scaled fp16 copies of q, k, v, dO
 int launch_fp16_copies(const BwdArgs& a, int64_t S, void* stream);
+// One bf16 tensor -> exact fp16 copy scaled by 2^-exps[0] (forward: V)
+int launch_fp16_copy1(const void* src, void* dst, int64_t elems, unsigned* amax_bits, int* exps,
+                      void* stream);
 int launch_dq_convert(const BwdArgs& a, int64_t S, int dtype, void* stream);
 int launch_permute(const SegTable& t, int B, int H, int d, int dtype, int to_natural,
                    const void* in, void* out, void* stream);

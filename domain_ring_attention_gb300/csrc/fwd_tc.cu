@@ -17,12 +17,18 @@
 //                  O_t += P_t V     (tcgen05.mma, A = P from TMEM, B from smem)
 //   warps 4-7    softmax for query half 0, warps 8-11 for half 1: read S_t from
 //                TMEM, mask (shard tails, causal / zigzag order), online
-//                softmax in the log2 domain, write P_t (bf16) back over S_t,
+//                softmax in the log2 domain, write P_t (fp16) back over S_t,
 //                rescale O_t when the running max grows by more than 2^8, and
 //                finally normalise O_t and store out / lse.
 // Tensor memory: S_0 | S_1 | O_0 | O_1 (128 + 128 + D + D of 512 columns).
+// S = Q K^T runs on the bf16 inputs.  O += P V runs in fp16: P (<= 2^8 with the
+// stale-max rescaling) keeps 11 significant bits instead of bf16's 8, and V is
+// an exact fp16 copy scaled by a power of two (made before the launch).  The
+// output error is then ~8x below that of a bf16 P, which also matters for
+// the backward's Delta = rowsum(dO o out).
 // Every barrier wait is bounded (see tc_ptx.cuh).
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include <cmath>
 #include <algorithm>
@@ -45,6 +51,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;   // rescale O only when the max grows by > 2^8
 constexpr int kMaxOrder = 4096;        // longest tile order passed as a kernel parameter
+// d = 64: part of the exponentials go to the FMA pipe (see exp2_poly_pair)
+template <int D>
+constexpr bool kPolyExp = D == 64;
 
 template <int D>
 struct Cfg {
@@ -76,6 +85,7 @@ struct FwdParams {
     float scale_log2;          // softmax scale * log2(e)
     int causal;
     int out_f32;
+    const int* exps;           // exps[0]: v16 = v * 2^-exps[0]
     int use_order;             // causal: CTAs take tiles heaviest first
     uint16_t order[kMaxOrder];
 };
@@ -92,6 +102,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
@@ -212,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             // so that while one softmax warpgroup works on S_t, the tensor core
             // runs the other half's PV and next S.
             constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kN, 0, 0);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kM, D, 0, 1);
+            constexpr uint32_t idesc_o = idesc_f16_f32(kM, D, 0, 1);     // P and V in fp16
             auto issue_s = [&](int t, int s) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -345,14 +360,22 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     for (int i = 0; i < 16; ++i) {
                         const uint64_t x = ffma2(f2_pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
                                                  sl2x2, negm2);
-                        float x0, x1;
-                        f2_unpack(x, x0, x1);
-                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        float p0, p1;
+                        if (kPolyExp<D> && (i & 7) == 7) {
+                            // d = 64: one pair in eight on the FMA pipe (the
+                            // MUFU alone would run exactly at the tensor rate)
+                            exp2_poly_pair(x, p0, p1);
+                        } else {
+                            float x0, x1;
+                            f2_unpack(x, x0, x1);
+                            p0 = ex2(x0);
+                            p1 = ex2(x1);
+                        }
                         if (i & 1)
                             acc1 = fadd2(acc1, f2_pack(p0, p1));
                         else
                             acc0 = fadd2(acc0, f2_pack(p0, p1));
-                        pk[i] = pack_bf16(p0, p1);
+                        pk[i] = pack_f16(p0, p1);
                     }
                     tmem_st16(tS + c * 16, pk);
                 }
@@ -386,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         if (ok && j > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_o(t), (j - 1) & 1, abort_flag));
         if (ok) {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            // O holds P (V * 2^-e_v): undo the fp16 scaling of V with the normalisation
+            const float inv = l > 0.f ? ldexpf(1.f, p.exps[0]) / l : 0.f;
             const int64_t grow = qt.row0 + kM * t + row;
             const int64_t off = (((int64_t)b * p.tab.S + grow) * H + h) * D;
 #pragma unroll
@@ -449,14 +473,15 @@ EncodeTiledFn get_encode() {
 }
 
 // BSHD bf16 tensor as a 4-D map (d, H, S, B), box (64, 1, 128, 1), 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int d) {
+bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int d,
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)S * H * d * 2};
     const cuuint32_t box[4] = {64, 1, 128, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+    return enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -467,7 +492,7 @@ int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
     FwdParams p;
     const int S = (int)L.S;
     if (!make_map(&p.tq, a.q, a.B, S, a.H, D) || !make_map(&p.tk, a.k, a.B, S, a.H, D) ||
-        !make_map(&p.tv, a.v, a.B, S, a.H, D))
+        !make_map(&p.tv, a.v16, a.B, S, a.H, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
         return (int)cudaErrorInvalidValue;
     fill_segtable(L, kNQ * kM, &p.tab);
     // Longest-processing-time-first order for causal work: a 256-row unit
@@ -492,6 +517,7 @@ int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
     }
     p.out = a.out;
     p.out_f32 = a.out_dtype == ST_DTYPE_F32 ? 1 : 0;
+    p.exps = a.exps;
     p.lse = a.lse;
     p.B = a.B;
     p.H = a.H;

@@ -166,6 +166,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
            ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with fp16 A and B (format 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem desc] * B[smem desc]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -225,6 +231,34 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+
+// 2^x for two values on the FMA pipe instead of the MUFU (x <= 126; values
+// below -126 are clamped, giving ~1e-38 instead of 0).  Range reduction in
+// the Cody-Waite manner: n = round(x) by the 1.5 * 2^23 shifter, f = x - n in
+// [-1/2, 1/2], 2^f by a degree-3 polynomial fitted here for minimum relative
+// error on [-1/2, 1/2] (max relative error 7.5e-5, far below the 2^-9 of the
+// bf16 P it feeds), then 2^n added to the exponent field with one integer
+// multiply-add.
+__device__ __forceinline__ void exp2_poly_pair(uint64_t x2, float& p0, float& p1) {
+    float x0, x1;
+    f2_unpack(x2, x0, x1);
+    const uint64_t xc = f2_pack(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
+    const uint64_t shifter = f2_pack(12582912.f, 12582912.f);
+    const uint64_t neg_shifter = f2_pack(-12582912.f, -12582912.f);
+    const uint64_t minus1 = f2_pack(-1.f, -1.f);
+    const uint64_t t = fadd2(xc, shifter);       // round(x) in the low mantissa bits
+    const uint64_t n = fadd2(t, neg_shifter);    // round(x) as a float (exact)
+    const uint64_t f = ffma2(n, minus1, xc);     // x - round(x) (exact)
+    uint64_t p = ffma2(f, f2_pack(0.05517605319619179f, 0.05517605319619179f),
+                       f2_pack(0.24261149764060974f, 0.24261149764060974f));
+    p = ffma2(p, f, f2_pack(0.6932601928710938f, 0.6932601928710938f));
+    p = ffma2(p, f, f2_pack(0.9999280571937561f, 0.9999280571937561f));
+    float q0, q1, t0, t1;
+    f2_unpack(p, q0, q1);
+    f2_unpack(t, t0, t1);
+    p0 = __uint_as_float(__float_as_uint(t0) * (1u << 23) + __float_as_uint(q0));
+    p1 = __uint_as_float(__float_as_uint(t1) * (1u << 23) + __float_as_uint(q1));
 }
 
 }  // namespace tc

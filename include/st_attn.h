@@ -90,7 +90,8 @@ int st_layout_query(const st_layout_t* layout, int64_t* S, int64_t* offsets, int
                     int* D, int* zigzag);
 
 /* Workspace bytes needed by st_attn_fwd (pass = 0) or st_attn_bwd (pass = 1)
- * for these sizes.  The forward needs none (the merge is fused).  The
+ * for these sizes.  The forward needs an fp16 copy of v [B,S,H,d] for bf16
+ * inputs and nothing for fp32 (the merge is fused).  The
  * backward needs an fp32 dQ accumulator [B,S,H,d] and the row sums Delta
  * [B,H,S]; bf16 adds four fp16 operand copies [B,S,H,d], fp32 adds the row
  * statistics in double [2,B,H,S]. */
@@ -106,7 +107,12 @@ int st_attn_workspace_size(const st_layout_t* layout, int B, int H, int d, int d
  *   out_dtype : dtype of out: the input dtype, or ST_DTYPE_F32 (the fp32
  *               accumulator normalised, without a final rounding to bf16).
  *   out       : [B,S,H,d] out_dtype;  lse : [B,H,S] fp32 (may not be NULL).
- *   workspace, ws_bytes : unused by the forward (may be NULL / 0). */
+ *   workspace : st_attn_workspace_size(pass=0) bytes of device memory,
+ *               16-byte aligned (bf16: the P V product runs in fp16 on an
+ *               exact copy of v scaled by a power of two, made here; fp32:
+ *               none, may be NULL / 0).
+ * Errors: ST_ERR_NULL, ST_ERR_UNSUPPORTED, ST_ERR_MISALIGNED,
+ *         ST_ERR_WORKSPACE, ST_ERR_INVALID_ARG, ST_ERR_CUDA. */
 int st_attn_fwd(const st_layout_t* layout, int B, int H, int d, int dtype, int causal,
                 float scale, const void* q, const void* k, const void* v, int out_dtype,
                 void* out, float* lse, void* workspace, size_t ws_bytes, void* stream);

@@ -72,6 +72,8 @@ def test_workspace_sizes(lib):
     lay = st.Layout([100, 150, 130, 132])
     n = ctypes.c_size_t()
     assert lib.st_attn_workspace_size(lay.handle, 1, 2, 64, 0, 0, ctypes.byref(n)) == 0 and n.value == 0
+    assert lib.st_attn_workspace_size(lay.handle, 1, 2, 64, 1, 0, ctypes.byref(n)) == 0
+    assert n.value >= 512 * 2 * 64 * 2
     assert lib.st_attn_workspace_size(lay.handle, 1, 2, 64, 0, 1, ctypes.byref(n)) == 0
     rows = 512 * 2
     assert n.value >= rows * 64 * 4 + rows * 4
@@ -88,12 +90,15 @@ def test_bad_calls_return_codes_without_a_gpu(lib):
     lse = P(0x20000)
     fwd = lib.st_attn_fwd
     assert fwd(None, 1, 1, 64, 1, 0, 0.0, good, good, good, 1, good, lse, None, 0, None) == -1
+    assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, good, good, good, 2, good, lse, good, 1 << 30, None) == -3
     assert fwd(lay.handle, 1, 1, 80, 1, 0, 0.0, good, good, good, 1, good, lse, None, 0, None) == -3
     assert fwd(lay.handle, 1, 1, 64, 5, 0, 0.0, good, good, good, 1, good, lse, None, 0, None) == -3
     assert fwd(lay.handle, 0, 1, 64, 1, 0, 0.0, good, good, good, 1, good, lse, None, 0, None) == -8
     assert fwd(lay.handle, 1, 1, 64, 1, 0, float("nan"), good, good, good, 1, good, lse, None, 0, None) == -8
     assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, None, good, good, 1, good, lse, None, 0, None) == -1
     assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, P(0x10008), good, good, 1, good, lse, None, 0, None) == -4
+    assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, good, good, good, 1, good, lse, None, 0, None) == -5
+    assert fwd(lay.handle, 1, 1, 64, 1, 0, 0.0, good, good, good, 1, good, lse, good, 64, None) == -5
     bwd = lib.st_attn_bwd
     qkv = [good] * 3
     assert bwd(lay.handle, 1, 1, 64, 1, 0, 0.0, *qkv, good, 1, lse, good, 1, good, good, good, None, 0, None) == -5
