@@ -51,8 +51,9 @@ struct Cfg {
     static constexpr int kVOff = kKOff + kTileBytes;
     static constexpr int kQOff = kVOff + kTileBytes;               // [stage] Q tiles
     static constexpr int kOOff = kQOff + kStages * kTileBytes;     // [stage] dO tiles
-    static constexpr int kSOff = kOOff + kStages * kTileBytes;     // dS^T, 128 x 128 fp16
-    static constexpr int kLOff = kSOff + 2 * kChunkBytes;          // [stage] lse*log2e, Delta
+    static constexpr int kSOff = kOOff + kStages * kTileBytes;     // dS^T (hi), 128 x 128 fp16
+    static constexpr int kS2Off = kSOff + 2 * kChunkBytes;         // dS^T lo part (partial tiles)
+    static constexpr int kLOff = kS2Off + 2 * kChunkBytes;         // [stage] lse*log2e, Delta
     static constexpr int kBarOff = kLOff + kStages * 2 * kT * 4;
     // kv_full, q_full[S], q_empty[S], s_full, ds_ready, it_done, dq_free, drain
     static constexpr int kNumBars = 6 + 2 * kStages;
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (sbase - raw);
     const uint32_t sK = sbase + C::kKOff, sV = sbase + C::kVOff, sQ = sbase + C::kQOff,
-                   sO = sbase + C::kOOff, sS = sbase + C::kSOff;
+                   sO = sbase + C::kOOff, sS = sbase + C::kSOff, sS2 = sbase + C::kS2Off;
     float* lse_s = reinterpret_cast<float*>(gbase + C::kLOff);   // [stage][2][128]
     const uint32_t bars = sbase + C::kBarOff;
     const uint32_t bar_kv = bars;
@@ -269,25 +270,46 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 ok = mbar_wait(bar_ds, i & 1, abort_flag);
                 if (!ok) return;
                 tc_fence_after();
-                // dV += P^T dO  (A: P^T bf16 in TMEM; B: dO, K = query rows, N = D)
+                // Partial (diagonal / ragged) tiles hold the pairs of rows and
+                // keys with few partners, whose P and dS are large: there both
+                // are split into fp16 hi + lo parts (P_lo in the consumed dP^T
+                // columns, dS_lo in a second smem tile) and every product gets
+                // a second MMA for the lo part.
+                const bool split = classify(causal, natq, nq, kt.nat0, kt.nq, kT) == kPartial;
+                // dV += P^T dO  (A: P^T fp16 in TMEM; B: dO, K = query rows, N = D)
 #pragma unroll
                 for (int kk = 0; kk < kT / 16; ++kk)
                     mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
                            smem_desc_sw128(o_t + kk * 2048, C::kChunkBytes, 1024), id_kv,
                            (i > 0 || kk > 0) ? 1u : 0u);
-                // dK += dS^T Q  (A: dS^T K-major in smem; B: Q, K = query rows, N = D)
+                if (split) {
 #pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk) {
-                    const uint32_t aoff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::kColDK, smem_desc_sw128(sS + aoff, 16, 1024),
-                           smem_desc_sw128(q_t + kk * 2048, C::kChunkBytes, 1024), id_kv,
-                           (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kT / 16; ++kk)
+                        mma_ts(tmem + C::kColDV, tmem + C::kColDP + kk * 8,
+                               smem_desc_sw128(o_t + kk * 2048, C::kChunkBytes, 1024), id_kv, 1u);
                 }
-                // dQ_t = dS K  (A: dS, M = query rows contiguous; B: K, K = keys, N = D)
+                // dK += dS^T Q  (A: dS^T K-major in smem; B: Q, K = query rows, N = D)
+                for (int part = 0; part < (split ? 2 : 1); ++part) {
+                    const uint32_t a_t = part == 0 ? sS : sS2;
 #pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk)
-                    mma_ss(tmem + C::kColDP, smem_desc_sw128(sS + kk * 2048, C::kChunkBytes, 1024),
-                           smem_desc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), id_q, kk > 0);
+                    for (int kk = 0; kk < kT / 16; ++kk) {
+                        const uint32_t aoff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                        mma_ss(tmem + C::kColDK, smem_desc_sw128(a_t + aoff, 16, 1024),
+                               smem_desc_sw128(q_t + kk * 2048, C::kChunkBytes, 1024), id_kv,
+                               (i > 0 || kk > 0 || part > 0) ? 1u : 0u);
+                    }
+                }
+                // dQ_t = dS K  (A: dS, M = query rows contiguous; B: K, K = keys, N = D).
+                // It overwrites the P_lo columns, which the dV MMA above read
+                // first (tcgen05.mma operations of one thread run in order).
+                for (int part = 0; part < (split ? 2 : 1); ++part) {
+                    const uint32_t a_t = part == 0 ? sS : sS2;
+#pragma unroll
+                    for (int kk = 0; kk < kT / 16; ++kk)
+                        mma_ss(tmem + C::kColDP, smem_desc_sw128(a_t + kk * 2048, C::kChunkBytes, 1024),
+                               smem_desc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), id_q,
+                               (kk > 0 || part > 0) ? 1u : 0u);
+                }
                 mma_commit(bar_it);
                 mma_commit(bar_qe(s));
                 ++i;
@@ -305,7 +327,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const float dp_mul = ldexpf(1.f, p.exps[2] + p.exps[3]);           // dP' -> dP
         const float ds_mul = ldexpf(1.f, -p.exps[4] - kPShift);            // P' (dP - Delta) -> dS'
         // dS^T row r: two 128-byte-swizzled 64-column chunks
-        const uint32_t ds_row = sS + (uint32_t)r * 128;
         int i = 0;
         bool ok = true;
         ring_walk_q(p.tab, kt.shard, [&](int, int nq, int natq) {
@@ -320,13 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             // query column c is visible to this key iff c < nq, r < nk and natk <= natq + c
             const int cmin = (kind == kFull) ? 0 : (causal ? max(0, natk - natq) : 0);
             const bool row_ok = r < kt.nq;
+            const bool split = kind == kPartial;   // hi + lo parts (see the MMA issuer)
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 uint32_t sv[32], dv[32];
                 tmem_ld32(lane_base + C::kColS + c4 * 32, sv);
                 tmem_ld32(lane_base + C::kColDP + c4 * 32, dv);
                 tmem_wait_ld();
-                uint32_t pp[16], dd[16];
+                uint32_t pp[16], dd[16], pl[16], dl[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     float pv[2], dsv[2];
@@ -340,15 +362,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     }
                     pp[e] = pack_f16(pv[0], pv[1]);
                     dd[e] = pack_f16(dsv[0], dsv[1]);
+                    if (split) {
+                        const float2 ph = __half22float2(*reinterpret_cast<const __half2*>(&pp[e]));
+                        const float2 dh = __half22float2(*reinterpret_cast<const __half2*>(&dd[e]));
+                        pl[e] = pack_f16(pv[0] - ph.x, pv[1] - ph.y);
+                        dl[e] = pack_f16(dsv[0] - dh.x, dsv[1] - dh.y);
+                    }
                 }
+                // P^T chunk -> S columns already read; P_lo -> dP^T columns already read
                 tmem_st16(lane_base + C::kColS + c4 * 16, pp);
+                if (split) tmem_st16(lane_base + C::kColDP + c4 * 16, pl);
                 // dS^T columns c4*32 .. +31 = 16-byte units 4*(c4&1) .. +3 of chunk c4>>1
-                const uint32_t chunk = ds_row + (uint32_t)(c4 >> 1) * C::kChunkBytes;
+                const uint32_t coff = (uint32_t)r * 128 + (uint32_t)(c4 >> 1) * C::kChunkBytes;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const uint32_t unit = (uint32_t)((c4 & 1) * 4 + u);
-                    st_shared_v4(chunk + ((unit ^ (uint32_t)(r & 7)) << 4), dd[4 * u], dd[4 * u + 1],
-                                 dd[4 * u + 2], dd[4 * u + 3]);
+                    const uint32_t at = coff + ((unit ^ (uint32_t)(r & 7)) << 4);
+                    st_shared_v4(sS + at, dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+                    if (split) st_shared_v4(sS2 + at, dl[4 * u], dl[4 * u + 1], dl[4 * u + 2], dl[4 * u + 3]);
                 }
             }
             tmem_wait_st();

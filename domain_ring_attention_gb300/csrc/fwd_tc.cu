@@ -237,19 +237,35 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
                 mma_commit(bar_s(t));
             };
-            auto issue_pv = [&](int t, int s, int jj) {
+            // Partial (diagonal / ragged) tiles carry the rows with few visible
+            // keys, whose P entries are large: there P = P_hi + P_lo (both
+            // fp16, P_lo in the upper 64 columns of the S region) and a
+            // second MMA adds P_lo V.
+            auto issue_pv = [&](int t, int s, int jj, bool split) {
 #pragma unroll
                 for (int kk = 0; kk < kN / 16; ++kk)
                     mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
                            smem_desc_sw128(sV + s * C::kTileBytes + kk * 2048, C::kChunkBytes, 1024),
                            idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                if (split) {
+#pragma unroll
+                    for (int kk = 0; kk < kN / 16; ++kk)
+                        mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kN / 2 + kk * 8,
+                               smem_desc_sw128(sV + s * C::kTileBytes + kk * 2048, C::kChunkBytes, 1024),
+                               idesc_o, 1u);
+                }
                 mma_commit(bar_o(t));
             };
             bool ok = mbar_wait(bar_q, 0, abort_flag);
             tc_fence_after();
             int j = 0;
+            bool split_prev[kNQ] = {false, false};
             ring_walk<kN>(p.tab, qt.shard, [&](int, int, int nk, int natk, bool) {
                 if (!ok || !active(nk, natk)) return;
+                bool split_cur[kNQ];
+#pragma unroll
+                for (int t = 0; t < kNQ; ++t)
+                    split_cur[t] = half_kind(causal, nat_h[t], nq_h[t], natk, nk) == kPartial;
                 const int s = j % C::kStages;
                 ok = mbar_wait(bar_k(s), (j / C::kStages) & 1, abort_flag);
                 if (!ok) return;
@@ -263,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         ok = mbar_wait(bar_p(t), (j - 1) & 1, abort_flag);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_pv(t, sp, j - 1);
+                        issue_pv(t, sp, j - 1, split_prev[t]);
                         // S_t(j) overwrites P_t(j-1), which PV_t(j-1) reads: the
                         // tcgen05.mma operations of one thread execute in issue
                         // order, so S_t(j) can follow PV_t(j-1) without a wait.
@@ -272,6 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     if (!ok) return;
                     mma_commit(bar_e(sp));
                 }
+#pragma unroll
+                for (int t = 0; t < kNQ; ++t) split_prev[t] = split_cur[t];
                 ++j;
             });
             if (ok && j > 0) {
@@ -281,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     ok = mbar_wait(bar_p(t), (j - 1) & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv(t, sp, j - 1);
+                    issue_pv(t, sp, j - 1, split_prev[t]);
                 }
                 if (ok) mma_commit(bar_e(sp));
             }
@@ -353,15 +371,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const uint64_t sl2x2 = f2_pack(sl2, sl2);
                 const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
                 uint64_t acc0 = 0, acc1 = 0;   // two packed partial sums (0.0f bits)
+                // partial tiles: P = P_hi + P_lo, both fp16 (see issue_pv)
+                const bool split = kind == kPartial;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
+                    uint32_t pk[16], pl[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const uint64_t x = ffma2(f2_pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
                                                  sl2x2, negm2);
                         float p0, p1;
-                        if (kPolyExp<D> && (i & 7) == 7) {
+                        if (kPolyExp<D> && (i & 7) == 7 && !split) {
                             // d = 64: one pair in eight on the FMA pipe (the
                             // MUFU alone would run exactly at the tensor rate)
                             exp2_poly_pair(x, p0, p1);
@@ -376,8 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         else
                             acc0 = fadd2(acc0, f2_pack(p0, p1));
                         pk[i] = pack_f16(p0, p1);
+                        if (split) {
+                            const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
+                            pl[i] = pack_f16(p0 - hi.x, p1 - hi.y);
+                        }
                     }
                     tmem_st16(tS + c * 16, pk);
+                    if (split) tmem_st16(tS + kN / 2 + c * 16, pl);
                 }
                 float a0, a1, b0, b1;
                 f2_unpack(acc0, a0, a1);
