@@ -54,6 +54,8 @@ def parse():
                    help="override H (a smaller capture of the same sequence shape for ncu)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-train", action="store_true",
+                   help="skip the secondary forward+backward measurement on train_s32768")
     return p.parse_args()
 
 
@@ -178,6 +180,54 @@ def cpu_sample_tflops(wl, q, k, v, budget_s=12.0):
     return flops / dt / 1e12, rows_done, dt, cores
 
 
+def train_step_tflops(st, world, steps=3, warmup=2):
+    """Forward + backward on the training workload (B=2, H=32, d=128, S=32768,
+    causal zigzag over Dirichlet sharding shapes): one step = st_attn_fwd (fp32
+    out) + st_attn_bwd (fp32 gradients), inputs resident in HBM."""
+    wl = WORKLOADS["train_s32768"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v, do = make_inputs(wl, seed=7, device=dev, with_dout=True)
+    lay = st.Layout(wl.lens, wl.zigzag)
+    out = torch.empty(q.shape, device=dev, dtype=torch.float32)
+    lse = torch.empty((wl.B, wl.H, wl.S), device=dev, dtype=torch.float32)
+    wsf = torch.empty(st.st_attn_workspace_size(lay, wl.B, wl.H, wl.d, q.dtype, 0), device=dev,
+                      dtype=torch.uint8)
+    wsb = torch.empty(st.st_attn_workspace_size(lay, wl.B, wl.H, wl.d, q.dtype, 1), device=dev,
+                      dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        st.st_attn_fwd(lay, q, k, v, causal=True, out=out, lse=lse, stream=stream, workspace=wsf)
+
+    def bwd():
+        st.st_attn_bwd(lay, q, k, v, out, lse, do, causal=True, workspace=wsb, stream=stream)
+
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    tf = tb = 0.0
+    for _ in range(steps):
+        ev[0].record(stream)
+        fwd()
+        ev[1].record(stream)
+        bwd()
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        tf += ev[0].elapsed_time(ev[1])
+        tb += ev[1].elapsed_time(ev[2])
+    tf = max_over_ranks(tf / steps, world)
+    tb = max_over_ranks(tb / steps, world)
+    return {"workload": "train_s32768", "shard_lens": list(wl.lens), "causal": True, "zigzag": True,
+            "fwd_tflops": wl.fwd_flops() * world / (tf * 1e-3) / 1e12,
+            "bwd_tflops": wl.bwd_flops() * world / (tb * 1e-3) / 1e12,
+            "fwd_bwd_tflops": (wl.fwd_flops() + wl.bwd_flops()) * world / ((tf + tb) * 1e-3) / 1e12,
+            "fwd_ms": tf, "bwd_ms": tb,
+            "note": "fwd writes fp32 out (the backward's Delta); bwd writes fp32 dq, dk, dv"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -289,6 +339,8 @@ def run_ours(args, rank, world):
         e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
+    train = None if args.no_train else train_step_tflops(st, world)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         val, rows, dt, cores = cpu_sample_tflops(wl, q_h, k_h, v_h, budget_s=12.0)
@@ -314,6 +366,7 @@ def run_ours(args, rank, world):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
+            "secondary": train,
         }
         print(json.dumps(line), flush=True)
 

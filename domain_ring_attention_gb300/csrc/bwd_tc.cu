@@ -26,8 +26,10 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <vector>
 
 #include "device.cuh"
 #include "tc_ptx.cuh"
@@ -38,6 +40,7 @@ namespace {
 using namespace tc;
 
 constexpr int kT = 128;          // keys per CTA, rows per query tile
+constexpr int kMaxOrder = 4096;  // longest tile order passed as a kernel parameter
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -90,6 +93,8 @@ struct BwdParams {
     float scale_log2;
     int causal;
     int grad_f32;             // dK / dV written as fp32 (else bf16)
+    int use_order;            // causal: CTAs take key tiles heaviest first
+    uint16_t order[kMaxOrder];
 };
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -163,7 +168,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = p.H, S = p.tab.S;
     const int b = blockIdx.y / H, h = blockIdx.y % H;
-    const QTile kt = locate_qtile(p.tab, blockIdx.x, kT);    // this CTA's key tile
+    const int tile = p.use_order ? (int)p.order[blockIdx.x] : (int)blockIdx.x;
+    const QTile kt = locate_qtile(p.tab, tile, kT);           // this CTA's key tile
+    // Extra precision (hi + lo fp16 parts of P and dS) where gradients are
+    // large compared with their RMS: partial (diagonal / ragged) tiles, which
+    // hold the rows and keys with few partners, and under causal masking the
+    // key tile holding the first natural positions, which every query attends
+    // to (its dV and dK are orders of magnitude above the typical key's).
+    const bool lead_tile = p.causal && kt.nat0 < kT;
+    auto wants_split = [&](int kind) { return kind == kPartial || lead_tile; };
     const int causal = p.causal;
     auto active = [&](int nq, int natq) {
         return classify(causal, natq, nq, kt.nat0, kt.nq, kT) != kSkip;
@@ -275,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 // are split into fp16 hi + lo parts (P_lo in the consumed dP^T
                 // columns, dS_lo in a second smem tile) and every product gets
                 // a second MMA for the lo part.
-                const bool split = classify(causal, natq, nq, kt.nat0, kt.nq, kT) == kPartial;
+                const bool split = wants_split(classify(causal, natq, nq, kt.nat0, kt.nq, kT));
                 // dV += P^T dO  (A: P^T fp16 in TMEM; B: dO, K = query rows, N = D)
 #pragma unroll
                 for (int kk = 0; kk < kT / 16; ++kk)
@@ -341,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             // query column c is visible to this key iff c < nq, r < nk and natk <= natq + c
             const int cmin = (kind == kFull) ? 0 : (causal ? max(0, natk - natq) : 0);
             const bool row_ok = r < kt.nq;
-            const bool split = kind == kPartial;   // hi + lo parts (see the MMA issuer)
+            const bool split = wants_split(kind);   // hi + lo parts (see the MMA issuer)
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 uint32_t sv[32], dv[32];
@@ -515,6 +528,20 @@ int launch_t(const st_layout& L, const BwdArgs& a, void* stream) {
         !make_map(&p.tv, a.h16[2], a.B, S, a.H, D) || !make_map(&p.tdo, a.h16[3], a.B, S, a.H, D))
         return (int)cudaErrorInvalidValue;
     fill_segtable(L, kT, &p.tab);
+    // Longest-processing-time-first order for causal work: a key tile starting
+    // at natural position n is seen by about S - n query rows.
+    p.use_order = 0;
+    if (a.causal && p.tab.ntiles <= kMaxOrder) {
+        std::vector<std::pair<int, int>> w;
+        w.reserve(p.tab.ntiles);
+        for (int s = 0; s < p.tab.nseg; ++s)
+            for (int tl = p.tab.seg_tile[s]; tl < p.tab.seg_tile[s + 1]; ++tl)
+                w.emplace_back(p.tab.seg_nat[s] + (tl - p.tab.seg_tile[s]) * kT, tl);
+        std::stable_sort(w.begin(), w.end(),
+                         [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first < y.first; });
+        for (int i = 0; i < p.tab.ntiles; ++i) p.order[i] = (uint16_t)w[i].second;
+        p.use_order = 1;
+    }
     p.lse = a.lse;
     p.delta = a.delta;
     p.dq_acc = a.dq_acc;

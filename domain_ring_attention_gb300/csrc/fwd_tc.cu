@@ -32,6 +32,7 @@
 
 #include <cmath>
 #include <algorithm>
+#include <type_traits>
 #include <mutex>
 #include <vector>
 
@@ -371,39 +372,55 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const uint64_t sl2x2 = f2_pack(sl2, sl2);
                 const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
                 uint64_t acc0 = 0, acc1 = 0;   // two packed partial sums (0.0f bits)
-                // partial tiles: P = P_hi + P_lo, both fp16 (see issue_pv)
-                const bool split = kind == kPartial;
+                // Two compile-time variants of the exponential pass, so the full
+                // tiles run without the split code: partial tiles write
+                // P = P_hi + P_lo, both fp16 (see issue_pv) and use the MUFU only.
+                auto exp_pass = [&](auto split_tag) {
+                    constexpr bool kSplit = decltype(split_tag)::value;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16], pl[16];
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t pk[16], pl[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const uint64_t x = ffma2(f2_pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
-                                                 sl2x2, negm2);
-                        float p0, p1;
-                        if (kPolyExp<D> && (i & 7) == 7 && !split) {
-                            // d = 64: one pair in eight on the FMA pipe (the
-                            // MUFU alone would run exactly at the tensor rate)
-                            exp2_poly_pair(x, p0, p1);
-                        } else {
-                            float x0, x1;
-                            f2_unpack(x, x0, x1);
-                            p0 = ex2(x0);
-                            p1 = ex2(x1);
+                        for (int i = 0; i < 16; ++i) {
+                            const uint64_t x = ffma2(
+                                f2_pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2x2, negm2);
+                            float p0, p1;
+                            if constexpr (kPolyExp<D> && !kSplit) {
+                                if ((i & 7) == 7) {
+                                    // d = 64: one pair in eight on the FMA pipe
+                                    // (the MUFU alone would run exactly at the
+                                    // tensor rate)
+                                    exp2_poly_pair(x, p0, p1);
+                                } else {
+                                    float x0, x1;
+                                    f2_unpack(x, x0, x1);
+                                    p0 = ex2(x0);
+                                    p1 = ex2(x1);
+                                }
+                            } else {
+                                float x0, x1;
+                                f2_unpack(x, x0, x1);
+                                p0 = ex2(x0);
+                                p1 = ex2(x1);
+                            }
+                            if (i & 1)
+                                acc1 = fadd2(acc1, f2_pack(p0, p1));
+                            else
+                                acc0 = fadd2(acc0, f2_pack(p0, p1));
+                            pk[i] = pack_f16(p0, p1);
+                            if constexpr (kSplit) {
+                                const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
+                                pl[i] = pack_f16(p0 - hi.x, p1 - hi.y);
+                            }
                         }
-                        if (i & 1)
-                            acc1 = fadd2(acc1, f2_pack(p0, p1));
-                        else
-                            acc0 = fadd2(acc0, f2_pack(p0, p1));
-                        pk[i] = pack_f16(p0, p1);
-                        if (split) {
-                            const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
-                            pl[i] = pack_f16(p0 - hi.x, p1 - hi.y);
-                        }
+                        tmem_st16(tS + c * 16, pk);
+                        if constexpr (kSplit) tmem_st16(tS + kN / 2 + c * 16, pl);
                     }
-                    tmem_st16(tS + c * 16, pk);
-                    if (split) tmem_st16(tS + kN / 2 + c * 16, pl);
-                }
+                };
+                if (kind == kPartial)
+                    exp_pass(std::true_type{});
+                else
+                    exp_pass(std::false_type{});
                 float a0, a1, b0, b1;
                 f2_unpack(acc0, a0, a1);
                 f2_unpack(acc1, b0, b1);
