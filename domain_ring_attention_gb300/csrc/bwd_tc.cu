@@ -41,6 +41,7 @@ using namespace tc;
 
 constexpr int kT = 128;          // keys per CTA, rows per query tile
 constexpr int kMaxOrder = 4096;  // longest tile order passed as a kernel parameter
+constexpr int kFlush = 8;        // query tiles per TMEM accumulation segment (lead tile)
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -177,6 +178,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     // to (its dV and dK are orders of magnitude above the typical key's).
     const bool lead_tile = p.causal && kt.nat0 < kT;
     auto wants_split = [&](int kind) { return kind == kPartial || lead_tile; };
+    // fp32 gradients of the lead key tile: its dV and dK sum tens of thousands
+    // of products, and the tensor core's fp32 accumulation of that many terms
+    // drifts by ~1e-4 relative -- on the largest gradients of the tensor.  So
+    // every kFlush query tiles the TMEM accumulators are added into the fp32
+    // output rows (owned by this CTA) and the MMAs restart from zero.
+    const bool flush_tile = lead_tile && p.grad_f32;
+    auto seg_start = [&](int it) { return flush_tile ? (it % kFlush) == 0 : it == 0; };
     const int causal = p.causal;
     auto active = [&](int nq, int natq) {
         return classify(causal, natq, nq, kt.nat0, kt.nq, kT) != kSkip;
@@ -294,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 for (int kk = 0; kk < kT / 16; ++kk)
                     mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
                            smem_desc_sw128(o_t + kk * 2048, C::kChunkBytes, 1024), id_kv,
-                           (i > 0 || kk > 0) ? 1u : 0u);
+                           (!seg_start(i) || kk > 0) ? 1u : 0u);
                 if (split) {
 #pragma unroll
                     for (int kk = 0; kk < kT / 16; ++kk)
@@ -309,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         const uint32_t aoff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
                         mma_ss(tmem + C::kColDK, smem_desc_sw128(a_t + aoff, 16, 1024),
                                smem_desc_sw128(q_t + kk * 2048, C::kChunkBytes, 1024), id_kv,
-                               (i > 0 || kk > 0 || part > 0) ? 1u : 0u);
+                               (!seg_start(i) || kk > 0 || part > 0) ? 1u : 0u);
                     }
                 }
                 // dQ_t = dS K  (A: dS, M = query rows contiguous; B: K, K = keys, N = D).
@@ -337,6 +345,57 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         const int natk = kt.nat0 + r;
         const float sl2 = ldexpf(p.scale_log2, p.exps[0] + p.exps[1]);    // S' -> scaled log2 units
+        // Write (or, after a flush, add) this key row's dV and scale * dK from
+        // the TMEM accumulators into the outputs.
+        auto emit = [&](bool have, bool add) {
+            const int64_t off = (((int64_t)b * S + kt.row0 + r) * H + h) * D;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+                const float mul = which == 0 ? ldexpf(1.f, p.exps[3] - kPShift)
+                                             : ldexpf(p.scale, p.exps[4] + p.exps[0]);
+                void* dst = which == 0 ? p.dv : p.dk;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    if (have) {
+                        tmem_ld32(lane_base + col + c * 32, v);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = 0u;
+                    }
+                    if (r < kt.nq) {
+                        if (p.grad_f32) {
+                            float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(dst) + off + c * 32);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                float4 x = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
+                                                       __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
+                                if (add) {
+                                    const float4 y = d4[e];
+                                    x.x += y.x;
+                                    x.y += y.y;
+                                    x.z += y.z;
+                                    x.w += y.w;
+                                }
+                                d4[e] = x;
+                            }
+                        } else {
+                            uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + off + c * 32);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                d4[e] = make_uint4(
+                                    pack_bf16(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
+                                    pack_bf16(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
+                                    pack_bf16(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
+                                    pack_bf16(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
+                        }
+                    }
+                }
+            }
+        };
+        bool flushed = false;
         const float dp_mul = ldexpf(1.f, p.exps[2] + p.exps[3]);           // dP' -> dP
         const float ds_mul = ldexpf(1.f, -p.exps[4] - kPShift);            // P' (dP - Delta) -> dS'
         // dS^T row r: two 128-byte-swizzled 64-column chunks
@@ -344,6 +403,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         bool ok = true;
         ring_walk_q(p.tab, kt.shard, [&](int, int nq, int natq) {
             if (!ok || !active(nq, natq)) return;
+            if (flush_tile && i > 0 && (i % kFlush) == 0) {
+                // promote the finished segment (all MMAs of iteration i-1 done)
+                ok = __all_sync(0xffffffffu, mbar_wait(bar_it, (i - 1) & 1, abort_flag));
+                if (!ok) return;
+                tc_fence_after();
+                emit(true, flushed);
+                flushed = true;
+            }
             const int s = i % C::kStages;
             ok = __all_sync(0xffffffffu, mbar_wait(bar_qf(s), (i / C::kStages) & 1, abort_flag));
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_s, i & 1, abort_flag));
@@ -405,43 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         if (ok && i > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_it, (i - 1) & 1, abort_flag));
         if (ok) {
             tc_fence_after();
-            const int64_t off = (((int64_t)b * S + kt.row0 + r) * H + h) * D;
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
-                const float mul = which == 0 ? ldexpf(1.f, p.exps[3] - kPShift)
-                                             : ldexpf(p.scale, p.exps[4] + p.exps[0]);
-                void* dst = which == 0 ? p.dv : p.dk;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
-                    if (i > 0) {
-                        tmem_ld32(lane_base + col + c * 32, v);
-                        tmem_wait_ld();
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = 0u;
-                    }
-                    if (r < kt.nq) {
-                        if (p.grad_f32) {
-                            float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(dst) + off + c * 32);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                d4[e] = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
-                                                    __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
-                        } else {
-                            uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + off + c * 32);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                d4[e] = make_uint4(
-                                    pack_bf16(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
-                                    pack_bf16(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
-                                    pack_bf16(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
-                                    pack_bf16(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
-                        }
-                    }
-                }
-            }
+            emit(i > 0, flushed);
         }
     } else if (warp >= 8) {
         // ------------------------------------------------ dQ reduction (one query row per thread)

@@ -117,7 +117,9 @@ __device__ __forceinline__ int half_kind(int causal, int nat0, int nq, int natk,
     return classify(causal, nat0, nq, natk, nk, kN);
 }
 
-template <int D>
+// kSplit: compiled with the hi/lo path for partial tiles (causal masks or
+// ragged shards); layouts whose tiles are all full use the kernel without it.
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 bool split_cur[kNQ];
 #pragma unroll
                 for (int t = 0; t < kNQ; ++t)
-                    split_cur[t] = half_kind(causal, nat_h[t], nq_h[t], natk, nk) == kPartial;
+                    split_cur[t] = kSplit && half_kind(causal, nat_h[t], nq_h[t], natk, nk) == kPartial;
                 const int s = j % C::kStages;
                 ok = mbar_wait(bar_k(s), (j / C::kStages) & 1, abort_flag);
                 if (!ok) return;
@@ -408,19 +410,34 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             else
                                 acc0 = fadd2(acc0, f2_pack(p0, p1));
                             pk[i] = pack_f16(p0, p1);
-                            if constexpr (kSplit) {
-                                const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
-                                pl[i] = pack_f16(p0 - hi.x, p1 - hi.y);
-                            }
                         }
                         tmem_st16(tS + c * 16, pk);
-                        if constexpr (kSplit) tmem_st16(tS + kN / 2 + c * 16, pl);
+                        if constexpr (kSplit) {
+                            // second pass over the chunk for the lo parts: the
+                            // exponentials are recomputed (partial tiles only)
+                            // rather than kept alive next to the hi parts
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const uint64_t x = ffma2(
+                                    f2_pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2x2, negm2);
+                                float x0, x1;
+                                f2_unpack(x, x0, x1);
+                                const float p0 = ex2(x0), p1 = ex2(x1);
+                                const float2 hi = __half22float2(__floats2half2_rn(p0, p1));
+                                pl[i] = pack_f16(p0 - hi.x, p1 - hi.y);
+                            }
+                            tmem_st16(tS + kN / 2 + c * 16, pl);
+                        }
                     }
                 };
-                if (kind == kPartial)
-                    exp_pass(std::true_type{});
-                else
+                if constexpr (kSplit) {
+                    if (kind == kPartial)
+                        exp_pass(std::true_type{});
+                    else
+                        exp_pass(std::false_type{});
+                } else {
                     exp_pass(std::false_type{});
+                }
                 float a0, a1, b0, b1;
                 f2_unpack(acc0, a0, a1);
                 f2_unpack(acc1, b0, b1);
@@ -528,7 +545,7 @@ bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int d,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool kSplit>
 int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
     using C = Cfg<D>;
     FwdParams p;
@@ -565,7 +582,7 @@ int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
     p.H = a.H;
     p.scale_log2 = a.scale * kLog2e;
     p.causal = a.causal;
-    auto kern = fwd_tc_kernel<D>;
+    auto kern = fwd_tc_kernel<D, kSplit>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return (int)e;
     dim3 grid(p.tab.ntiles, a.B * a.H);
@@ -577,7 +594,13 @@ int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
 
 int launch_fwd_tc(const st_layout& L, const AttnArgs& a, void* stream, bool* handled) {
     *handled = true;
-    return a.d == 64 ? launch_t<64>(L, a, stream) : launch_t<128>(L, a, stream);
+    // partial tiles exist under causal masking or when a segment is not a
+    // multiple of the 128-row tile
+    bool split = a.causal != 0;
+    for (size_t s = 0; s + 1 < L.seg_buf.size(); ++s)
+        split |= ((L.seg_buf[s + 1] - L.seg_buf[s]) % kN) != 0;
+    if (a.d == 64) return split ? launch_t<64, true>(L, a, stream) : launch_t<64, false>(L, a, stream);
+    return split ? launch_t<128, true>(L, a, stream) : launch_t<128, false>(L, a, stream);
 }
 
 int fwd_tc_device_error(bool clear) {
