@@ -22,7 +22,7 @@ ST_MAX_SHARDS = 32
 ERRORS = {
     0: "ST_OK", -1: "ST_ERR_NULL", -2: "ST_ERR_INVALID_LAYOUT", -3: "ST_ERR_UNSUPPORTED",
     -4: "ST_ERR_MISALIGNED", -5: "ST_ERR_WORKSPACE", -6: "ST_ERR_CUDA",
-    -7: "ST_ERR_DEVICE_TIMEOUT", -8: "ST_ERR_INVALID_ARG",
+    -7: "ST_ERR_DEVICE_TIMEOUT", -8: "ST_ERR_INVALID_ARG", -9: "ST_ERR_SCRATCH_LIMIT",
 }
 
 # C prototypes: (name, restype, argtypes)
@@ -38,6 +38,7 @@ PROTOTYPES = [
                              ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     ("st_attn_workspace_size", _I, [_P, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     ("st_attn_fwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P, _SZ, _P]),
+    ("st_attn_fwd_noalloc", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P]),
     ("st_attn_fwd_partials", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P]),
     ("st_attn_merge", _I, [_I, _I, _I, _I64, _I, _P, _P, _P, _P, _I, _P]),
     ("st_attn_bwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P, _P, _I, _P, _P, _P,

@@ -43,6 +43,7 @@ extern "C" const char* st_error_string(int code) {
         case ST_ERR_CUDA: return "CUDA error (see st_last_cuda_error)";
         case ST_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
         case ST_ERR_INVALID_ARG: return "an argument is out of range";
+        case ST_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed 32 MiB scratch of st_attn_fwd_noalloc";
         default: return "unknown status";
     }
 }
@@ -77,6 +78,8 @@ BwdWorkspace bwd_workspace_layout(int64_t rows, int d, int dtype) {
     w.total = off;
     return w;
 }
+
+int record_cuda_error(int err) { return cuda_status(err); }
 
 size_t fwd_workspace_bytes(int64_t rows, int d, int dtype) {
     if (dtype != ST_DTYPE_BF16) return 0;

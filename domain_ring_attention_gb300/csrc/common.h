@@ -63,6 +63,8 @@ struct AttnArgs {
 
 // Workspace of st_attn_fwd: bf16 needs the fp16 copy of v plus 256 bytes.
 size_t fwd_workspace_bytes(int64_t rows, int d, int dtype);
+// Records a CUDA error code for st_last_cuda_error and returns ST_ERR_CUDA (0 -> ST_OK).
+int record_cuda_error(int err);
 
 struct BwdArgs {
     const void* q;

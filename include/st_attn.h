@@ -56,7 +56,8 @@ enum {
     ST_ERR_WORKSPACE = -5,       /* workspace NULL or smaller than required         */
     ST_ERR_CUDA = -6,            /* a CUDA runtime call or launch failed            */
     ST_ERR_DEVICE_TIMEOUT = -7,  /* a bounded device-side wait gave up              */
-    ST_ERR_INVALID_ARG = -8      /* B, H, S, D or another size is out of range      */
+    ST_ERR_INVALID_ARG = -8,     /* B, H, S, D or another size is out of range      */
+    ST_ERR_SCRATCH_LIMIT = -9    /* problem too large for st_attn_fwd_noalloc       */
 };
 
 enum { ST_DTYPE_F32 = 0, ST_DTYPE_BF16 = 1 };
@@ -116,6 +117,32 @@ int st_attn_workspace_size(const st_layout_t* layout, int B, int H, int d, int d
 int st_attn_fwd(const st_layout_t* layout, int B, int H, int d, int dtype, int causal,
                 float scale, const void* q, const void* k, const void* v, int out_dtype,
                 void* out, float* lse, void* workspace, size_t ws_bytes, void* stream);
+
+/* Forward for callers that cannot allocate device memory.  No passage of the
+ * paper corresponds to it: it is an interface for callers that are handed
+ * only their input and output buffers (an operator running inside another
+ * runtime), whose memory is fixed at start-up (real-time or certified loops
+ * that forbid allocation afterwards), or whose critical path must not call a
+ * device allocator (allocations can synchronise and can fail).
+ * It computes exactly what st_attn_fwd computes, but the workspace is a
+ * fixed 32 MiB array of device memory inside this library instead of a
+ * caller buffer:
+ *   - every GPU that loads the library holds the array until the process
+ *     exits; nothing is allocated or freed per call;
+ *   - problems whose workspace (st_attn_workspace_size, pass 0) exceeds
+ *     32 MiB are refused with ST_ERR_SCRATCH_LIMIT before anything runs
+ *     (bf16: B * S * H * d must stay below about 16.7 million);
+ *   - the first call on a device, made with that device current, looks up
+ *     the array's device address; make that first call before any stream
+ *     capture;
+ *   - every call on a device uses the same array, so calls whose GPU work
+ *     overlaps (on different streams, or from different host threads) race
+ *     and must be ordered by the caller.  The array keeps the last call's
+ *     contents; whatever a call needs zeroed, it zeroes itself.
+ * Other arguments, layouts and errors: as st_attn_fwd (no workspace). */
+int st_attn_fwd_noalloc(const st_layout_t* layout, int B, int H, int d, int dtype, int causal,
+                        float scale, const void* q, const void* k, const void* v, int out_dtype,
+                        void* out, float* lse, void* stream);
 
 /* Forward that stops short of the merge: for every query row and every KV
  * shard j it writes the partial (O_j normalised by its own sum, lse_j) over
