@@ -54,6 +54,8 @@ def parse():
                    help="override H (a smaller capture of the same sequence shape for ncu)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--bwd", action="store_true",
+                   help="time forward (fp32 out) + backward (fp32 gradients) as the step")
     p.add_argument("--no-train", action="store_true",
                    help="skip the secondary forward+backward measurement on train_s32768")
     return p.parse_args()
@@ -270,16 +272,26 @@ def run_ours(args, rank, world):
     q_h, k_h, v_h = make_inputs(wl, seed=rank, device="cpu")
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
     lay = st.Layout(wl.lens, wl.zigzag)
-    out = torch.empty_like(q)
+    out = torch.empty(q.shape, device=dev, dtype=torch.float32 if args.bwd else q.dtype)
     lse = torch.empty((wl.B, wl.H, wl.S), device=dev, dtype=torch.float32)
     ws = torch.empty(max(1, st.st_attn_workspace_size(lay, wl.B, wl.H, wl.d, q.dtype, 0)),
                      device=dev, dtype=torch.uint8)
     stream = torch.cuda.current_stream()
     # kernels of one forward step: bf16 -> max|v|, fp16 copy of v, fused forward
     launches_per_step = 3 if q.dtype == torch.bfloat16 else 1
+    flops = wl.fwd_flops()
+    if args.bwd:
+        do = make_inputs(wl, seed=1000 + rank, device=dev, with_dout=True)[3]
+        wsb = torch.empty(st.st_attn_workspace_size(lay, wl.B, wl.H, wl.d, q.dtype, 1), device=dev,
+                          dtype=torch.uint8)
+        flops += wl.bwd_flops()
+        # backward: Delta, max|x| of four tensors, their fp16 copies, the fused backward
+        launches_per_step += 4 if q.dtype == torch.bfloat16 else 2
 
     def step():
         st.st_attn_fwd(lay, q, k, v, causal=wl.causal, out=out, lse=lse, stream=stream, workspace=ws)
+        if args.bwd:
+            st.st_attn_bwd(lay, q, k, v, out, lse, do, causal=wl.causal, workspace=wsb, stream=stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -304,7 +316,6 @@ def run_ours(args, rank, world):
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_per_step = total_ms / args.steps
-    flops = wl.fwd_flops()
     value = flops * world / (ms_per_step * 1e-3) / 1e12
     peak_b, peak_s, hbm, peak_kind = peaks()
     achieved = flops / (statistics.mean(launch_ms) * 1e-3) / 1e12
