@@ -29,6 +29,7 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 #include <vector>
 
 #include "device.cuh"
@@ -224,11 +225,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 tma_load_4d(sV + c * C::kChunkBytes, &p.tv, bar_kv, c * 64, h, kt.row0, b);
             }
         }
+        // Row statistics staged per query tile, in the form the softmax uses:
+        //   [0, kT):   kPShift - lse * log2(e)   (-inf for rows past the tile)
+        //   [kT, 2kT): -Delta * 2^-(e_dS + kPShift)
+        const float ds_mul = ldexpf(1.f, -p.exps[4] - kPShift);
         int i = 0;
         bool ok = true;
         ring_walk_q(p.tab, kt.shard, [&](int q0, int nq, int natq) {
             if (!ok || !active(nq, natq)) return;
             const int s = i % C::kStages;
+            // fetched before the stage is free, so the global loads overlap the wait
+            float nl[kT / 32], nd[kT / 32];
+#pragma unroll
+            for (int e = 0; e < kT / 32; ++e) {
+                const int r = e * 32 + lane;
+                const bool valid = r < nq;
+                nl[e] = valid ? (float)kPShift - p.lse[lse_base + q0 + r] * kLog2e : -INFINITY;
+                nd[e] = valid ? -p.delta[lse_base + q0 + r] * ds_mul : 0.f;
+            }
             if (i >= C::kStages)
                 ok = __all_sync(0xffffffffu, mbar_wait(bar_qe(s), ((i / C::kStages) - 1) & 1, abort_flag));
             if (!ok) return;
@@ -243,10 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             float* ls = lse_s + s * 2 * kT;
 #pragma unroll
             for (int e = 0; e < kT / 32; ++e) {
-                const int r = e * 32 + lane;
-                const bool valid = r < nq;
-                ls[r] = valid ? p.lse[lse_base + q0 + r] * kLog2e - (float)kPShift : INFINITY;
-                ls[kT + r] = valid ? p.delta[lse_base + q0 + r] : 0.f;
+                ls[e * 32 + lane] = nl[e];
+                ls[kT + e * 32 + lane] = nd[e];
             }
             mbar_arrive(bar_qf(s));
             ++i;
@@ -269,9 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             ring_walk_q(p.tab, kt.shard, [&](int, int nq, int natq) {
                 if (!ok || !active(nq, natq)) return;
                 const int s = i % C::kStages;
+                // S^T(i) overwrites P^T(i-1) and dP^T(i) overwrites P_lo(i-1),
+                // both read by MMAs of iteration i-1 issued earlier (the
+                // tcgen05.mma operations of one thread run in issue order); the
+                // dP^T columns also hold dQ_t(i-1), so dP^T(i) waits for its drain.
                 ok = mbar_wait(bar_qf(s), (i / C::kStages) & 1, abort_flag);
-                if (ok && i > 0) ok = mbar_wait(bar_it, (i - 1) & 1, abort_flag);
-                if (ok && i > 0) ok = mbar_wait(bar_dqf, (i - 1) & 1, abort_flag);
                 if (!ok) return;
                 tc_fence_after();
                 const uint32_t q_t = sQ + s * C::kTileBytes, o_t = sO + s * C::kTileBytes;
@@ -280,6 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                     const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
                     mma_ss(tmem + C::kColS, smem_desc_sw128(sK + off, 16, 1024),
                            smem_desc_sw128(q_t + off, 16, 1024), id_s, kk > 0);
+                }
+                if (i > 0) {
+                    ok = mbar_wait(bar_dqf, (i - 1) & 1, abort_flag);
+                    if (!ok) return;
+                    tc_fence_after();
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -320,6 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                                (!seg_start(i) || kk > 0 || part > 0) ? 1u : 0u);
                     }
                 }
+                // Q(i) and dO(i) are read by no later MMA: the producer may refill
+                // the stage while dQ_t runs.
+                mma_commit(bar_qe(s));
                 // dQ_t = dS K  (A: dS, M = query rows contiguous; B: K, K = keys, N = D).
                 // It overwrites the P_lo columns, which the dV MMA above read
                 // first (tcgen05.mma operations of one thread run in order).
@@ -332,7 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                                (kk > 0 || part > 0) ? 1u : 0u);
                 }
                 mma_commit(bar_it);
-                mma_commit(bar_qe(s));
                 ++i;
             });
             mma_commit(bar_drain);
@@ -396,9 +417,75 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             }
         };
         bool flushed = false;
-        const float dp_mul = ldexpf(1.f, p.exps[2] + p.exps[3]);           // dP' -> dP
-        const float ds_mul = ldexpf(1.f, -p.exps[4] - kPShift);            // P' (dP - Delta) -> dS'
-        // dS^T row r: two 128-byte-swizzled 64-column chunks
+        // dS' = P' (dP - Delta) 2^-(e_dS + kPShift), with the power of two
+        // folded into dP's multiplier and into the staged -Delta
+        const float dpm = ldexpf(1.f, p.exps[2] + p.exps[3] - p.exps[4] - kPShift);
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), dpm2 = f2_pack(dpm, dpm);
+        // One query tile.  Compile-time variants: kMask (partial tiles: the
+        // causal diagonal and ragged key tiles need a per-element mask; query
+        // columns past the tile end are zeroed by their -inf statistic) and
+        // kLo (hi + lo fp16 parts of P and dS, see the MMA issuer).
+        auto tile_pass = [&](auto mask_tag, auto lo_tag, const float* ls, int cmin) {
+            constexpr bool kMask = decltype(mask_tag)::value;
+            constexpr bool kLo = decltype(lo_tag)::value;
+            const bool row_ok = r < kt.nq;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t sv[32], dv[32];
+                tmem_ld32(lane_base + C::kColS + c4 * 32, sv);
+                tmem_ld32(lane_base + C::kColDP + c4 * 32, dv);
+                tmem_wait_ld();
+                uint32_t pp[16], dd[16], pl[16], dl[16];
+#pragma unroll
+                for (int e2 = 0; e2 < 8; ++e2) {
+                    // statistics of columns c .. c+3 (broadcast shared loads)
+                    const int c = c4 * 32 + 4 * e2;
+                    const float4 nl = *reinterpret_cast<const float4*>(ls + c);
+                    const float4 nd = *reinterpret_cast<const float4*>(ls + kT + c);
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int e = 2 * e2 + h2;
+                        const uint64_t nl2 = h2 ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y);
+                        const uint64_t nd2 = h2 ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y);
+                        float x0, x1;
+                        f2_unpack(ffma2(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sl2x2, nl2),
+                                  x0, x1);
+                        float p0 = ex2(x0), p1 = ex2(x1);
+                        if constexpr (kMask) {
+                            // query column cc is visible to this key iff cc >= cmin (and the key row exists)
+                            if (!row_ok || c + 2 * h2 < cmin) p0 = 0.f;
+                            if (!row_ok || c + 2 * h2 + 1 < cmin) p1 = 0.f;
+                        }
+                        const uint64_t p2 = f2_pack(p0, p1);
+                        const uint64_t t2 =
+                            ffma2(f2_pack(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), dpm2, nd2);
+                        float d0, d1;
+                        f2_unpack(fmul2(p2, t2), d0, d1);
+                        pp[e] = pack_f16(p0, p1);
+                        dd[e] = pack_f16(d0, d1);
+                        if constexpr (kLo) {
+                            const float2 ph = __half22float2(*reinterpret_cast<const __half2*>(&pp[e]));
+                            const float2 dh = __half22float2(*reinterpret_cast<const __half2*>(&dd[e]));
+                            pl[e] = pack_f16(p0 - ph.x, p1 - ph.y);
+                            dl[e] = pack_f16(d0 - dh.x, d1 - dh.y);
+                        }
+                    }
+                }
+                // P^T chunk -> S columns already read; P_lo -> dP^T columns already read
+                tmem_st16(lane_base + C::kColS + c4 * 16, pp);
+                if constexpr (kLo) tmem_st16(lane_base + C::kColDP + c4 * 16, pl);
+                // dS^T columns c4*32 .. +31 = 16-byte units 4*(c4&1) .. +3 of chunk c4>>1
+                const uint32_t coff = (uint32_t)r * 128 + (uint32_t)(c4 >> 1) * C::kChunkBytes;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t unit = (uint32_t)((c4 & 1) * 4 + u);
+                    const uint32_t at = coff + ((unit ^ (uint32_t)(r & 7)) << 4);
+                    st_shared_v4(sS + at, dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+                    if constexpr (kLo)
+                        st_shared_v4(sS2 + at, dl[4 * u], dl[4 * u + 1], dl[4 * u + 2], dl[4 * u + 3]);
+                }
+            }
+        };
         int i = 0;
         bool ok = true;
         ring_walk_q(p.tab, kt.shard, [&](int, int nq, int natq) {
@@ -418,49 +505,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             tc_fence_after();
             const float* ls = lse_s + s * 2 * kT;
             const int kind = classify(causal, natq, nq, kt.nat0, kt.nq, kT);
-            // query column c is visible to this key iff c < nq, r < nk and natk <= natq + c
-            const int cmin = (kind == kFull) ? 0 : (causal ? max(0, natk - natq) : 0);
-            const bool row_ok = r < kt.nq;
-            const bool split = wants_split(kind);   // hi + lo parts (see the MMA issuer)
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t sv[32], dv[32];
-                tmem_ld32(lane_base + C::kColS + c4 * 32, sv);
-                tmem_ld32(lane_base + C::kColDP + c4 * 32, dv);
-                tmem_wait_ld();
-                uint32_t pp[16], dd[16], pl[16], dl[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pv[2], dsv[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int c = c4 * 32 + 2 * e + u;
-                        const bool vis = row_ok && c >= cmin;   // c >= nq is killed by lse = +inf
-                        const float pr = vis ? ex2(fmaf(__uint_as_float(sv[2 * e + u]), sl2, -ls[c])) : 0.f;
-                        pv[u] = pr;
-                        dsv[u] = pr * fmaf(__uint_as_float(dv[2 * e + u]), dp_mul, -ls[kT + c]) * ds_mul;
-                    }
-                    pp[e] = pack_f16(pv[0], pv[1]);
-                    dd[e] = pack_f16(dsv[0], dsv[1]);
-                    if (split) {
-                        const float2 ph = __half22float2(*reinterpret_cast<const __half2*>(&pp[e]));
-                        const float2 dh = __half22float2(*reinterpret_cast<const __half2*>(&dd[e]));
-                        pl[e] = pack_f16(pv[0] - ph.x, pv[1] - ph.y);
-                        dl[e] = pack_f16(dsv[0] - dh.x, dsv[1] - dh.y);
-                    }
-                }
-                // P^T chunk -> S columns already read; P_lo -> dP^T columns already read
-                tmem_st16(lane_base + C::kColS + c4 * 16, pp);
-                if (split) tmem_st16(lane_base + C::kColDP + c4 * 16, pl);
-                // dS^T columns c4*32 .. +31 = 16-byte units 4*(c4&1) .. +3 of chunk c4>>1
-                const uint32_t coff = (uint32_t)r * 128 + (uint32_t)(c4 >> 1) * C::kChunkBytes;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t unit = (uint32_t)((c4 & 1) * 4 + u);
-                    const uint32_t at = coff + ((unit ^ (uint32_t)(r & 7)) << 4);
-                    st_shared_v4(sS + at, dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
-                    if (split) st_shared_v4(sS2 + at, dl[4 * u], dl[4 * u + 1], dl[4 * u + 2], dl[4 * u + 3]);
-                }
+            if (kind == kPartial) {
+                // causal: query column c sees key natk iff natk <= natq + c
+                const int cmin = causal ? max(0, natk - natq) : 0;
+                tile_pass(std::true_type{}, std::true_type{}, ls, cmin);
+            } else if (lead_tile) {
+                tile_pass(std::false_type{}, std::true_type{}, ls, 0);
+            } else {
+                tile_pass(std::false_type{}, std::false_type{}, ls, 0);
             }
             tmem_wait_st();
             fence_proxy_async();

@@ -20,7 +20,9 @@
 //                softmax in the log2 domain, write P_t (fp16) back over S_t,
 //                rescale O_t when the running max grows by more than 2^8, and
 //                finally normalise O_t and store out / lse.
-// Tensor memory: S_0 | S_1 | O_0 | O_1 (128 + 128 + D + D of 512 columns).
+// Tensor memory: S_0 | S_1 | O_0 | O_1 (128 + 128 + D + D of 512 columns; at
+// d = 64 each O carries 16 more columns, the first of which accumulates the
+// row sums of P through a column of ones beside V).
 // S = Q K^T runs on the bf16 inputs.  O += P V runs in fp16: P (<= 2^8 with the
 // stale-max rescaling) keeps 11 significant bits instead of bf16's 8, and V is
 // an exact fp16 copy scaled by a power of two (made before the launch).  The
@@ -52,9 +54,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;   // rescale O only when the max grows by > 2^8
 constexpr int kMaxOrder = 4096;        // longest tile order passed as a kernel parameter
-// d = 64: part of the exponentials go to the FMA pipe (see exp2_poly_pair)
-template <int D>
-constexpr bool kPolyExp = D == 64;
 
 template <int D>
 struct Cfg {
@@ -62,17 +61,38 @@ struct Cfg {
     static constexpr int kChunkBytes = kM * 128;           // 128 rows x 64 bf16
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     static constexpr int kStages = D == 64 ? 4 : 2;
+    // d = 64: the row sums of P come out of the P V product itself.  Each V
+    // stage carries a second 64-column swizzle atom (at the descriptor's
+    // leading byte offset) whose column 0 is all ones, the MMA runs with
+    // N = 80, and O's column 64 accumulates sum_j P_ij -- the sum of exactly
+    // the fp16 P values that weight V -- with no per-score add in the softmax.
+    // (d = 128 has no TMEM left for the extra 2 x 16 columns.)
+    static constexpr bool kSumCol = D == 64;
+    static constexpr int kOCols = D + (kSumCol ? 16 : 0);
+    static constexpr int kVStageBytes = kTileBytes + (kSumCol ? kChunkBytes : 0);
+    // d = 64: Q is kept in tensor memory as the A operand of S = Q K^T, so
+    // the S MMAs read only K from shared memory (an SS MMA of N = 128 reads
+    // 8 KB of shared memory per K step, close to the 128 B/clk the SM's
+    // shared memory delivers while the tensor core needs ~73 clocks for it).
+    static constexpr bool kQTmem = D == 64;
     static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQOff + kNQ * kTileBytes;
+    static constexpr int kKOff = kQOff + (kQTmem ? 0 : kNQ * kTileBytes);
     static constexpr int kVOff = kKOff + kStages * kTileBytes;
-    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kStages * kVStageBytes;
     // q_full, k_full[S], v_full[S], kv_empty[S], s_full[NQ], p_full[NQ], o_done[NQ], drain
     static constexpr int kNumBars = 2 + 3 * kStages + 3 * kNQ;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     static constexpr uint32_t kTmemCols = 512;
+    static_assert(kNQ * kN + kNQ * kOCols + (kQTmem ? kNQ * D / 2 : 0) <= (int)kTmemCols,
+                  "tensor memory columns");
     __host__ __device__ static constexpr uint32_t s_col(int t) { return (uint32_t)(t * kN); }
-    __host__ __device__ static constexpr uint32_t o_col(int t) { return (uint32_t)(kNQ * kN + t * D); }
+    __host__ __device__ static constexpr uint32_t o_col(int t) { return (uint32_t)(kNQ * kN + t * kOCols); }
+    // Q_t as bf16 pairs: column c holds elements 2c and 2c + 1 of the row
+    __host__ __device__ static constexpr uint32_t q_col(int t) {
+        return (uint32_t)(kNQ * kN + kNQ * kOCols + t * (D / 2));
+    }
 };
 
 struct FwdParams {
@@ -80,6 +100,7 @@ struct FwdParams {
     CUtensorMap tk;
     CUtensorMap tv;
     SegTable tab;              // query tiles of kNQ * kM rows
+    const void* q;             // bf16 [B,S,H,D] (read directly when Q lives in TMEM)
     void* out;                 // bf16, or fp32 when out_f32
     float* lse;
     int B, H;
@@ -90,6 +111,16 @@ struct FwdParams {
     int use_order;             // causal: CTAs take tiles heaviest first
     uint16_t order[kMaxOrder];
 };
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
@@ -159,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     };
 
     if (threadIdx.x == 0) {
-        mbar_init(bar_q, 1);
+        mbar_init(bar_q, C::kQTmem ? kNQ * kM : 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar_k(s), 1);
             mbar_init(bar_v(s), 1);
@@ -183,6 +214,23 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         prefetch_tmap(&p.tk);
         prefetch_tmap(&p.tv);
     }
+    if constexpr (C::kSumCol) {
+        // The ones atom of every V stage, in the 128-byte-swizzled MN-major
+        // layout of the V tiles: key row r is 128 bytes at r * 128, and its
+        // 16-byte unit u sits at unit position u ^ (r & 7).  Column 0 (unit 0,
+        // first half) is 1.0 in fp16, every other column 0.
+        if (warp == 2 || warp == 3) {
+            const int t = threadIdx.x - 64;                 // 0..63
+            for (int s = 0; s < C::kStages; ++s) {
+                uint4* atom = reinterpret_cast<uint4*>(gbase + C::kVOff + s * C::kVStageBytes + C::kTileBytes);
+                for (int u = t; u < C::kChunkBytes / 16; u += 64) {
+                    const int r = u >> 3, pos = u & 7;      // row r, unit position pos
+                    atom[u] = make_uint4(pos == (r & 7) ? 0x3C00u : 0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async();                            // visible to the tensor core
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -191,11 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar_q, kNQ * C::kTileBytes);
-            for (int t = 0; t < kNQ; ++t)
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &p.tq, bar_q, c * 64, h,
-                                qt.row0 + kM * t, b);
+            if constexpr (!C::kQTmem) {
+                mbar_arrive_expect_tx(bar_q, kNQ * C::kTileBytes);
+                for (int t = 0; t < kNQ; ++t)
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_4d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &p.tq, bar_q, c * 64, h,
+                                    qt.row0 + kM * t, b);
+            }
             int j = 0;
             bool ok = true;
             ring_walk<kN>(p.tab, qt.shard, [&](int, int kv0, int nk, int natk, bool) {
@@ -209,12 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                 kv0, b);
                 mbar_arrive_expect_tx(bar_v(s), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(sV + s * C::kTileBytes + c * C::kChunkBytes, &p.tv, bar_v(s), c * 64, h,
+                    tma_load_4d(sV + s * C::kVStageBytes + c * C::kChunkBytes, &p.tv, bar_v(s), c * 64, h,
                                 kv0, b);
                 ++j;
             });
             // Let every load this thread issued land before the CTA can exit.
-            mbar_wait(bar_q, 0, abort_flag);
+            if constexpr (!C::kQTmem) mbar_wait(bar_q, 0, abort_flag);
             for (int jj = max(0, j - C::kStages); jj < j; ++jj) {
                 const int s = jj % C::kStages;
                 const uint32_t ph = (jj / C::kStages) & 1;
@@ -230,13 +280,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             // so that while one softmax warpgroup works on S_t, the tensor core
             // runs the other half's PV and next S.
             constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kN, 0, 0);
-            constexpr uint32_t idesc_o = idesc_f16_f32(kM, D, 0, 1);     // P and V in fp16
+            constexpr uint32_t idesc_o = idesc_f16_f32(kM, C::kOCols, 0, 1);   // P and V in fp16
             auto issue_s = [&](int t, int s) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::s_col(t), smem_desc_sw128(sQ + t * C::kTileBytes + off, 16, 1024),
-                           smem_desc_sw128(sK + s * C::kTileBytes + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                    if constexpr (C::kQTmem)
+                        mma_ts(tmem + C::s_col(t), tmem + C::q_col(t) + kk * 8,
+                               smem_desc_sw128(sK + s * C::kTileBytes + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                    else
+                        mma_ss(tmem + C::s_col(t), smem_desc_sw128(sQ + t * C::kTileBytes + off, 16, 1024),
+                               smem_desc_sw128(sK + s * C::kTileBytes + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar_s(t));
             };
@@ -248,13 +302,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                 for (int kk = 0; kk < kN / 16; ++kk)
                     mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
-                           smem_desc_sw128(sV + s * C::kTileBytes + kk * 2048, C::kChunkBytes, 1024),
+                           smem_desc_sw128(sV + s * C::kVStageBytes + kk * 2048, C::kChunkBytes, 1024),
                            idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
                 if (split) {
 #pragma unroll
                     for (int kk = 0; kk < kN / 16; ++kk)
                         mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kN / 2 + kk * 8,
-                               smem_desc_sw128(sV + s * C::kTileBytes + kk * 2048, C::kChunkBytes, 1024),
+                               smem_desc_sw128(sV + s * C::kVStageBytes + kk * 2048, C::kChunkBytes, 1024),
                                idesc_o, 1u);
                 }
                 mma_commit(bar_o(t));
@@ -321,6 +375,24 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         const int nq = nq_h[t];
         const int natq = nat_h[t] + row;
         const float sl2 = p.scale_log2;
+        if constexpr (C::kQTmem) {
+            // this thread's Q row -> TMEM (rows past the tile end are zero)
+            uint32_t qr[D / 2];
+            const int64_t goff = (((int64_t)b * p.tab.S + qt.row0 + kM * t + row) * H + h) * D;
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + goff);
+#pragma unroll
+            for (int u = 0; u < D / 8; ++u) {
+                const uint4 x = row < nq ? src[u] : make_uint4(0u, 0u, 0u, 0u);
+                qr[4 * u] = x.x;
+                qr[4 * u + 1] = x.y;
+                qr[4 * u + 2] = x.z;
+                qr[4 * u + 3] = x.w;
+            }
+            tmem_st32(lane_base + C::q_col(t), qr);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar_q);
+        }
         float m = -INFINITY, l = 0.f;
         int j = 0;
         bool ok = true;
@@ -376,9 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 uint64_t acc0 = 0, acc1 = 0;   // two packed partial sums (0.0f bits)
                 // Two compile-time variants of the exponential pass, so the full
                 // tiles run without the split code: partial tiles write
-                // P = P_hi + P_lo, both fp16 (see issue_pv) and use the MUFU only.
+                // P = P_hi + P_lo, both fp16 (see issue_pv).
                 auto exp_pass = [&](auto split_tag) {
-                    constexpr bool kSplit = decltype(split_tag)::value;
+                    constexpr bool kLo = decltype(split_tag)::value;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t pk[16], pl[16];
@@ -386,33 +458,19 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         for (int i = 0; i < 16; ++i) {
                             const uint64_t x = ffma2(
                                 f2_pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2x2, negm2);
-                            float p0, p1;
-                            if constexpr (kPolyExp<D> && !kSplit) {
-                                if ((i & 7) == 7) {
-                                    // d = 64: one pair in eight on the FMA pipe
-                                    // (the MUFU alone would run exactly at the
-                                    // tensor rate)
-                                    exp2_poly_pair(x, p0, p1);
-                                } else {
-                                    float x0, x1;
-                                    f2_unpack(x, x0, x1);
-                                    p0 = ex2(x0);
-                                    p1 = ex2(x1);
-                                }
-                            } else {
-                                float x0, x1;
-                                f2_unpack(x, x0, x1);
-                                p0 = ex2(x0);
-                                p1 = ex2(x1);
+                            float x0, x1;
+                            f2_unpack(x, x0, x1);
+                            const float p0 = ex2(x0), p1 = ex2(x1);
+                            if constexpr (!C::kSumCol) {   // d = 64 sums in the MMA
+                                if (i & 1)
+                                    acc1 = fadd2(acc1, f2_pack(p0, p1));
+                                else
+                                    acc0 = fadd2(acc0, f2_pack(p0, p1));
                             }
-                            if (i & 1)
-                                acc1 = fadd2(acc1, f2_pack(p0, p1));
-                            else
-                                acc0 = fadd2(acc0, f2_pack(p0, p1));
                             pk[i] = pack_f16(p0, p1);
                         }
                         tmem_st16(tS + c * 16, pk);
-                        if constexpr (kSplit) {
+                        if constexpr (kLo) {
                             // second pass over the chunk for the lo parts: the
                             // exponentials are recomputed (partial tiles only)
                             // rather than kept alive next to the hi parts
@@ -439,9 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     exp_pass(std::false_type{});
                 }
                 float a0, a1, b0, b1;
-                f2_unpack(acc0, a0, a1);
-                f2_unpack(acc1, b0, b1);
-                l = l * alpha + ((a0 + a1) + (b0 + b1));
+                if constexpr (!C::kSumCol) {
+                    f2_unpack(acc0, a0, a1);
+                    f2_unpack(acc1, b0, b1);
+                    l = l * alpha + ((a0 + a1) + (b0 + b1));
+                }
                 m = m_use;
             }
             if (__any_sync(0xffffffffu, resc) && j > 0) {
@@ -458,6 +518,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
                         tmem_st32(tO + c * 32, r);
                     }
+                    if constexpr (C::kSumCol) {   // the row-sum column scales with O
+                        uint32_t r[16];
+                        tmem_ld16(tO + D, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st16(tO + D, r);
+                    }
                 }
             }
             tmem_wait_st();
@@ -468,6 +536,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         if (ok && j > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_o(t), (j - 1) & 1, abort_flag));
         if (ok) {
             tc_fence_after();
+            if constexpr (C::kSumCol) {   // l = sum_j P_ij from O's extra column
+                uint32_t r[16];
+                tmem_ld16(tO + D, r);
+                tmem_wait_ld();
+                l = j > 0 ? __uint_as_float(r[0]) : 0.f;
+            }
             // O holds P (V * 2^-e_v): undo the fp16 scaling of V with the normalisation
             const float inv = l > 0.f ? ldexpf(1.f, p.exps[0]) / l : 0.f;
             const int64_t grow = qt.row0 + kM * t + row;
@@ -574,6 +648,7 @@ int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
         for (int i = 0; i < p.tab.ntiles; ++i) p.order[i] = (uint16_t)w[i].second;
         p.use_order = 1;
     }
+    p.q = a.q;
     p.out = a.out;
     p.out_f32 = a.out_dtype == ST_DTYPE_F32 ? 1 : 0;
     p.exps = a.exps;

@@ -232,33 +232,10 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
-
-// 2^x for two values on the FMA pipe instead of the MUFU (x <= 126; values
-// below -126 are clamped, giving ~1e-38 instead of 0).  Range reduction in
-// the Cody-Waite manner: n = round(x) by the 1.5 * 2^23 shifter, f = x - n in
-// [-1/2, 1/2], 2^f by a degree-3 polynomial fitted here for minimum relative
-// error on [-1/2, 1/2] (max relative error 7.5e-5, far below the 2^-9 of the
-// bf16 P it feeds), then 2^n added to the exponent field with one integer
-// multiply-add.
-__device__ __forceinline__ void exp2_poly_pair(uint64_t x2, float& p0, float& p1) {
-    float x0, x1;
-    f2_unpack(x2, x0, x1);
-    const uint64_t xc = f2_pack(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
-    const uint64_t shifter = f2_pack(12582912.f, 12582912.f);
-    const uint64_t neg_shifter = f2_pack(-12582912.f, -12582912.f);
-    const uint64_t minus1 = f2_pack(-1.f, -1.f);
-    const uint64_t t = fadd2(xc, shifter);       // round(x) in the low mantissa bits
-    const uint64_t n = fadd2(t, neg_shifter);    // round(x) as a float (exact)
-    const uint64_t f = ffma2(n, minus1, xc);     // x - round(x) (exact)
-    uint64_t p = ffma2(f, f2_pack(0.05517605319619179f, 0.05517605319619179f),
-                       f2_pack(0.24261149764060974f, 0.24261149764060974f));
-    p = ffma2(p, f, f2_pack(0.6932601928710938f, 0.6932601928710938f));
-    p = ffma2(p, f, f2_pack(0.9999280571937561f, 0.9999280571937561f));
-    float q0, q1, t0, t1;
-    f2_unpack(p, q0, q1);
-    f2_unpack(t, t0, t1);
-    p0 = __uint_as_float(__float_as_uint(t0) * (1u << 23) + __float_as_uint(q0));
-    p1 = __uint_as_float(__float_as_uint(t1) * (1u << 23) + __float_as_uint(q1));
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
 
 }  // namespace tc
