@@ -11,9 +11,10 @@
 // log-sum-exp merge of the per-shard partials, done incrementally.
 //
 // Warp roles (384 threads):
-//   warp 0       TMA producer: Q once, then K and V tiles into a smem ring.
+//   warp 0       TMA producer: Q (d = 128) once, then K and V tiles into a
+//                smem ring.
 //   warp 1       TMEM allocator and single-thread MMA issuer:
-//                  S_t = Q_t K^T    (tcgen05.mma, A and B from smem)
+//                  S_t = Q_t K^T    (tcgen05.mma; Q from TMEM at d = 64, else smem)
 //                  O_t += P_t V     (tcgen05.mma, A = P from TMEM, B from smem)
 //   warps 4-7    softmax for query half 0, warps 8-11 for half 1: read S_t from
 //                TMEM, mask (shard tails, causal / zigzag order), online
@@ -274,23 +275,32 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
+        // Issue order on the tensor pipe (ping-pong of the two halves):
+        //   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) ...
+        // so that while one softmax warpgroup works on S_t, the tensor core
+        // runs the other half's PV and next S, and the two warpgroups stay
+        // staggered.  S_t(j+1) overwrites P_t(j), which PV_t(j) reads: the
+        // tcgen05.mma operations of one thread execute in issue order, so it
+        // needs no wait.  The loop is kept lean (descriptors precomputed, a
+        // stage or K step adds its byte offset >> 4 to the start-address
+        // field): at d = 64 the tensor core runs a tile's 24 MMAs in ~1150
+        // clocks, little more than a thread needs to issue them.
         if (lane == 0) {
-            // Issue order on the tensor pipe (ping-pong of the two halves):
-            //   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) ...
-            // so that while one softmax warpgroup works on S_t, the tensor core
-            // runs the other half's PV and next S.
             constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kN, 0, 0);
             constexpr uint32_t idesc_o = idesc_f16_f32(kM, C::kOCols, 0, 1);   // P and V in fp16
-            auto issue_s = [&](int t, int s) {
+            const uint64_t kdesc = smem_desc_sw128(sK, 16, 1024);
+            const uint64_t vdesc = smem_desc_sw128(sV, C::kChunkBytes, 1024);
+            const uint64_t qdesc = smem_desc_sw128(sQ, 16, 1024);
+            auto issue_s = [&](int t, uint64_t kd) {
+                const uint32_t tS = tmem + C::s_col(t);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                    const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
                     if constexpr (C::kQTmem)
-                        mma_ts(tmem + C::s_col(t), tmem + C::q_col(t) + kk * 8,
-                               smem_desc_sw128(sK + s * C::kTileBytes + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                        mma_ts(tS, tmem + C::q_col(t) + kk * 8, kd + off, idesc_s, kk > 0 ? 1u : 0u);
                     else
-                        mma_ss(tmem + C::s_col(t), smem_desc_sw128(sQ + t * C::kTileBytes + off, 16, 1024),
-                               smem_desc_sw128(sK + s * C::kTileBytes + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                        mma_ss(tS, qdesc + (uint64_t)((t * C::kTileBytes) >> 4) + off, kd + off, idesc_s,
+                               kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar_s(t));
             };
@@ -298,18 +308,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             // keys, whose P entries are large: there P = P_hi + P_lo (both
             // fp16, P_lo in the upper 64 columns of the S region) and a
             // second MMA adds P_lo V.
-            auto issue_pv = [&](int t, int s, int jj, bool split) {
+            auto issue_pv = [&](int t, uint64_t vd, int jj, bool split) {
+                const uint32_t tS = tmem + C::s_col(t), tO = tmem + C::o_col(t);
 #pragma unroll
                 for (int kk = 0; kk < kN / 16; ++kk)
-                    mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
-                           smem_desc_sw128(sV + s * C::kVStageBytes + kk * 2048, C::kChunkBytes, 1024),
-                           idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tO, tS + kk * 8, vd + (uint64_t)(kk * 128), idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
                 if (split) {
 #pragma unroll
                     for (int kk = 0; kk < kN / 16; ++kk)
-                        mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kN / 2 + kk * 8,
-                               smem_desc_sw128(sV + s * C::kVStageBytes + kk * 2048, C::kChunkBytes, 1024),
-                               idesc_o, 1u);
+                        mma_ts(tO, tS + kN / 2 + kk * 8, vd + (uint64_t)(kk * 128), idesc_o, 1u);
                 }
                 mma_commit(bar_o(t));
             };
@@ -324,23 +331,22 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 for (int t = 0; t < kNQ; ++t)
                     split_cur[t] = kSplit && half_kind(causal, nat_h[t], nq_h[t], natk, nk) == kPartial;
                 const int s = j % C::kStages;
+                const uint64_t kd = kdesc + (uint64_t)(s * (C::kTileBytes >> 4));
                 ok = mbar_wait(bar_k(s), (j / C::kStages) & 1, abort_flag);
                 if (!ok) return;
                 tc_fence_after();
                 if (j == 0) {
-                    for (int t = 0; t < kNQ; ++t) issue_s(t, s);
+                    for (int t = 0; t < kNQ; ++t) issue_s(t, kd);
                 } else {
                     const int sp = (j - 1) % C::kStages;
+                    const uint64_t vd = vdesc + (uint64_t)(sp * (C::kVStageBytes >> 4));
                     ok = mbar_wait(bar_v(sp), ((j - 1) / C::kStages) & 1, abort_flag);
                     for (int t = 0; t < kNQ && ok; ++t) {
                         ok = mbar_wait(bar_p(t), (j - 1) & 1, abort_flag);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_pv(t, sp, j - 1, split_prev[t]);
-                        // S_t(j) overwrites P_t(j-1), which PV_t(j-1) reads: the
-                        // tcgen05.mma operations of one thread execute in issue
-                        // order, so S_t(j) can follow PV_t(j-1) without a wait.
-                        issue_s(t, s);
+                        issue_pv(t, vd, j - 1, split_prev[t]);
+                        issue_s(t, kd);
                     }
                     if (!ok) return;
                     mma_commit(bar_e(sp));
@@ -351,12 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             });
             if (ok && j > 0) {
                 const int sp = (j - 1) % C::kStages;
+                const uint64_t vd = vdesc + (uint64_t)(sp * (C::kVStageBytes >> 4));
                 ok = mbar_wait(bar_v(sp), ((j - 1) / C::kStages) & 1, abort_flag);
                 for (int t = 0; t < kNQ && ok; ++t) {
                     ok = mbar_wait(bar_p(t), (j - 1) & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv(t, sp, j - 1, split_prev[t]);
+                    issue_pv(t, vd, j - 1, split_prev[t]);
                 }
                 if (ok) mma_commit(bar_e(sp));
             }
