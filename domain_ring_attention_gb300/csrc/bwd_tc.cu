@@ -264,9 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             ++i;
         });
         if (lane == 0) {
-            mbar_wait(bar_kv, 0, abort_flag);
+            // every load issued lands before the CTA can exit (also after an abort)
+            mbar_wait_drain(bar_kv, 0);
             for (int ii = max(0, i - C::kStages); ii < i; ++ii)
-                mbar_wait(bar_qf(ii % C::kStages), (ii / C::kStages) & 1, abort_flag);
+                mbar_wait_drain(bar_qf(ii % C::kStages), (ii / C::kStages) & 1);
         }
         (void)issued_tx;
     } else if (warp == 1) {
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 ++i;
             });
             mma_commit(bar_drain);
-            mbar_wait(bar_drain, 0, abort_flag);
+            mbar_wait_drain(bar_drain, 0);
         }
     } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------ softmax (one key row per thread)

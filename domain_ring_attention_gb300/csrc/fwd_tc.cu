@@ -264,13 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                 kv0, b);
                 ++j;
             });
-            // Let every load this thread issued land before the CTA can exit.
-            if constexpr (!C::kQTmem) mbar_wait(bar_q, 0, abort_flag);
+            // Let every load this thread issued land before the CTA can exit
+            // (also after an abort: the drain waits ignore the abort word).
+            if constexpr (!C::kQTmem) mbar_wait_drain(bar_q, 0);
             for (int jj = max(0, j - C::kStages); jj < j; ++jj) {
                 const int s = jj % C::kStages;
                 const uint32_t ph = (jj / C::kStages) & 1;
-                mbar_wait(bar_k(s), ph, abort_flag);
-                mbar_wait(bar_v(s), ph, abort_flag);
+                mbar_wait_drain(bar_k(s), ph);
+                mbar_wait_drain(bar_v(s), ph);
             }
         }
     } else if (warp == 1) {
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             }
             // Every MMA issued above must finish before the TMEM is released.
             mma_commit(bar_drain);
-            mbar_wait(bar_drain, 0, abort_flag);
+            mbar_wait_drain(bar_drain, 0);
         }
     } else if (warp >= 4) {
         // ------------------------------------------------ softmax + epilogue

@@ -74,6 +74,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Bounded wait used at kernel exit for this thread's own asynchronous work
+// (TMA loads it issued, MMAs it committed): it ignores the abort word, so a
+// CTA that gave up elsewhere still lets its copies and MMAs land before it
+// frees its shared and tensor memory, and it gives up after ~0.5 s.
+constexpr long long kDrainLimitCycles = 1000000000LL;
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 255u && clock64() - t0 > kDrainLimitCycles) {
+            atomicExch(&g_device_error, 1);
+            return false;
+        }
+    }
+}
+
 // 4-D tiled TMA load into shared memory, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, uint32_t bar, int c0,
                                             int c1, int c2, int c3) {
