@@ -80,8 +80,8 @@ struct Cfg {
     static constexpr int kKOff = kQOff + (kQTmem ? 0 : kNQ * kTileBytes);
     static constexpr int kVOff = kKOff + kStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kStages * kVStageBytes;
-    // q_full, k_full[S], v_full[S], kv_empty[S], s_full[NQ], p_full[NQ], o_done[NQ], drain
-    static constexpr int kNumBars = 2 + 3 * kStages + 3 * kNQ;
+    // q_full, kv_full[S], kv_empty[S], s_full[NQ], p_full[NQ], o_done[NQ], drain
+    static constexpr int kNumBars = 2 + 2 * kStages + 3 * kNQ;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -161,13 +161,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     const uint32_t sQ = sbase + C::kQOff, sK = sbase + C::kKOff, sV = sbase + C::kVOff;
     const uint32_t bars = sbase + C::kBarOff;
     const uint32_t bar_q = bars;
-    auto bar_k = [&](int s) { return bars + 8u * (1 + s); };
-    auto bar_v = [&](int s) { return bars + 8u * (1 + C::kStages + s); };
-    auto bar_e = [&](int s) { return bars + 8u * (1 + 2 * C::kStages + s); };
-    auto bar_s = [&](int t) { return bars + 8u * (1 + 3 * C::kStages + t); };
-    auto bar_p = [&](int t) { return bars + 8u * (1 + 3 * C::kStages + kNQ + t); };
-    auto bar_o = [&](int t) { return bars + 8u * (1 + 3 * C::kStages + 2 * kNQ + t); };
-    const uint32_t bar_drain = bars + 8u * (1 + 3 * C::kStages + 3 * kNQ);
+    // K and V of a tile land on one barrier: with the ring several tiles
+    // deep, both are there long before S needs K, and the MMA issuer polls
+    // one barrier per tile instead of two
+    auto bar_kv = [&](int s) { return bars + 8u * (1 + s); };
+    auto bar_e = [&](int s) { return bars + 8u * (1 + C::kStages + s); };
+    auto bar_s = [&](int t) { return bars + 8u * (1 + 2 * C::kStages + t); };
+    auto bar_p = [&](int t) { return bars + 8u * (1 + 2 * C::kStages + kNQ + t); };
+    auto bar_o = [&](int t) { return bars + 8u * (1 + 2 * C::kStages + 2 * kNQ + t); };
+    const uint32_t bar_drain = bars + 8u * (1 + 2 * C::kStages + 3 * kNQ);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kMiscOff + 4);
 
@@ -193,8 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (threadIdx.x == 0) {
         mbar_init(bar_q, C::kQTmem ? kNQ * kM : 1);
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(bar_k(s), 1);
-            mbar_init(bar_v(s), 1);
+            mbar_init(bar_kv(s), 1);
             mbar_init(bar_e(s), 1);
         }
         for (int t = 0; t < kNQ; ++t) {
@@ -254,13 +255,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const int s = j % C::kStages;
                 if (j >= C::kStages) ok = mbar_wait(bar_e(s), ((j / C::kStages) - 1) & 1, abort_flag);
                 if (!ok) return;
-                mbar_arrive_expect_tx(bar_k(s), C::kTileBytes);
+                mbar_arrive_expect_tx(bar_kv(s), 2 * C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(sK + s * C::kTileBytes + c * C::kChunkBytes, &p.tk, bar_k(s), c * 64, h,
+                    tma_load_4d(sK + s * C::kTileBytes + c * C::kChunkBytes, &p.tk, bar_kv(s), c * 64, h,
                                 kv0, b);
-                mbar_arrive_expect_tx(bar_v(s), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(sV + s * C::kVStageBytes + c * C::kChunkBytes, &p.tv, bar_v(s), c * 64, h,
+                    tma_load_4d(sV + s * C::kVStageBytes + c * C::kChunkBytes, &p.tv, bar_kv(s), c * 64, h,
                                 kv0, b);
                 ++j;
             });
@@ -270,8 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             for (int jj = max(0, j - C::kStages); jj < j; ++jj) {
                 const int s = jj % C::kStages;
                 const uint32_t ph = (jj / C::kStages) & 1;
-                mbar_wait_drain(bar_k(s), ph);
-                mbar_wait_drain(bar_v(s), ph);
+                mbar_wait_drain(bar_kv(s), ph);
             }
         }
     } else if (warp == 1) {
@@ -319,29 +318,27 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     for (int kk = 0; kk < kN / 16; ++kk)
                         mma_ts(tO, tS + kN / 2 + kk * 8, vd + (uint64_t)(kk * 128), idesc_o, 1u);
                 }
-                mma_commit(bar_o(t));
             };
             bool ok = mbar_wait(bar_q, 0, abort_flag);
             tc_fence_after();
             int j = 0;
             bool split_prev[kNQ] = {false, false};
-            ring_walk<kN>(p.tab, qt.shard, [&](int, int, int nk, int natk, bool) {
-                if (!ok || !active(nk, natk)) return;
-                bool split_cur[kNQ];
-#pragma unroll
-                for (int t = 0; t < kNQ; ++t)
-                    split_cur[t] = kSplit && half_kind(causal, nat_h[t], nq_h[t], natk, nk) == kPartial;
+            // One KV tile.  A tcgen05.commit costs the issuing thread about as
+            // much as an MMA, so there are three per tile: S_0, S_1 (each also
+            // covers the previous PV of its half, which the softmax relies on
+            // before rescaling O) and the stage release.
+            auto step = [&](bool split0, bool split1) {
                 const int s = j % C::kStages;
                 const uint64_t kd = kdesc + (uint64_t)(s * (C::kTileBytes >> 4));
-                ok = mbar_wait(bar_k(s), (j / C::kStages) & 1, abort_flag);
+                ok = mbar_wait(bar_kv(s), (j / C::kStages) & 1, abort_flag);
                 if (!ok) return;
                 tc_fence_after();
                 if (j == 0) {
                     for (int t = 0; t < kNQ; ++t) issue_s(t, kd);
                 } else {
+                    // V(j-1) landed with K(j-1), waited for one tile ago
                     const int sp = (j - 1) % C::kStages;
                     const uint64_t vd = vdesc + (uint64_t)(sp * (C::kVStageBytes >> 4));
-                    ok = mbar_wait(bar_v(sp), ((j - 1) / C::kStages) & 1, abort_flag);
                     for (int t = 0; t < kNQ && ok; ++t) {
                         ok = mbar_wait(bar_p(t), (j - 1) & 1, abort_flag);
                         if (!ok) break;
@@ -352,19 +349,30 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     if (!ok) return;
                     mma_commit(bar_e(sp));
                 }
-#pragma unroll
-                for (int t = 0; t < kNQ; ++t) split_prev[t] = split_cur[t];
+                split_prev[0] = split0;
+                split_prev[1] = split1;
                 ++j;
-            });
+            };
+            if constexpr (!kSplit) {
+                // every tile full and visible: the KV tiles are just counted
+                const int nkv = p.tab.S / kN;
+                for (int jj = 0; jj < nkv && ok; ++jj) step(false, false);
+            } else {
+                ring_walk<kN>(p.tab, qt.shard, [&](int, int, int nk, int natk, bool) {
+                    if (!ok || !active(nk, natk)) return;
+                    step(half_kind(causal, nat_h[0], nq_h[0], natk, nk) == kPartial,
+                         half_kind(causal, nat_h[1], nq_h[1], natk, nk) == kPartial);
+                });
+            }
             if (ok && j > 0) {
                 const int sp = (j - 1) % C::kStages;
                 const uint64_t vd = vdesc + (uint64_t)(sp * (C::kVStageBytes >> 4));
-                ok = mbar_wait(bar_v(sp), ((j - 1) / C::kStages) & 1, abort_flag);
                 for (int t = 0; t < kNQ && ok; ++t) {
                     ok = mbar_wait(bar_p(t), (j - 1) & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv(t, vd, j - 1, split_prev[t]);
+                    mma_commit(bar_o(t));   // the epilogue's single wait on O_t
                 }
                 if (ok) mma_commit(bar_e(sp));
             }
@@ -404,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         float m = -INFINITY, l = 0.f;
         int j = 0;
         bool ok = true;
-        ring_walk<kN>(p.tab, qt.shard, [&](int, int, int nk, int natk, bool) {
+        auto step = [&](int nk, int natk) {
             if (!ok || !active(nk, natk)) return;
             ok = __all_sync(0xffffffffu, mbar_wait(bar_s(t), j & 1, abort_flag));
             if (!ok) return;
@@ -513,10 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 m = m_use;
             }
             if (__any_sync(0xffffffffu, resc) && j > 0) {
-                // O_t must hold every previous PV product before it is rescaled
-                ok = __all_sync(0xffffffffu, mbar_wait(bar_o(t), (j - 1) & 1, abort_flag));
-                if (ok) {
-                    tc_fence_after();
+                // O_t already holds every previous PV product: PV_t(j-1) was
+                // issued before S_t(j), and the commit that signalled S_t(j)
+                // covers all earlier MMAs of the issuing thread
+                {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t r[32];
@@ -540,8 +548,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             tc_fence_before();
             mbar_arrive(bar_p(t));
             ++j;
-        });
-        if (ok && j > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_o(t), (j - 1) & 1, abort_flag));
+        };
+        if constexpr (!kSplit) {
+            // every tile full and visible (the issuer counts them the same way)
+            const int nkv = p.tab.S / kN;
+            for (int jj = 0; jj < nkv && ok; ++jj) step(kN, 0);
+        } else {
+            ring_walk<kN>(p.tab, qt.shard, [&](int, int, int nk, int natk, bool) { step(nk, natk); });
+        }
+        if (ok && j > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_o(t), 0, abort_flag));
         if (ok) {
             tc_fence_after();
             if constexpr (C::kSumCol) {   // l = sum_j P_ij from O's extra column
