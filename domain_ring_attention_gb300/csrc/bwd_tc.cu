@@ -19,9 +19,10 @@
 //   dQ  += scale dQ_t       (reduction warps: TMEM -> red.global.add.v4.f32)
 //
 // Warp roles (384 threads): warp 0 TMA producer (+ lse / Delta staging),
-// warp 1 TMEM allocator + MMA issuer, warps 4-7 softmax (one key row per
-// thread) and the dK / dV epilogue, warps 8-11 dQ reduction (one query row
-// per thread).  Tensor memory: S^T|P^T, dP^T|dQ_t, dV, dK.  Every barrier
+// warp 1 TMEM allocator + MMA issuer, warps 4-7 softmax for query columns
+// 0-63 (one key row per thread) and the dV epilogue, warps 8-11 softmax for
+// columns 64-127, the dK epilogue and the dQ reduction (one query row per
+// thread).  Tensor memory: S^T|P^T, dP^T|dQ_t, dV, dK.  Every barrier
 // wait is bounded (tc_ptx.cuh).
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -59,11 +60,15 @@ struct Cfg {
     static constexpr int kSOff = kOOff + kStages * kTileBytes;     // dS^T (hi), 128 x 128 fp16
     static constexpr int kS2Off = kSOff + 2 * kChunkBytes;         // dS^T lo part (partial tiles)
     static constexpr int kLOff = kS2Off + 2 * kChunkBytes;         // [stage] lse*log2e, Delta
-    static constexpr int kBarOff = kLOff + kStages * 2 * kT * 4;
+    // dQ staging: per reducer warp 32 rows x 32 fp32, rows padded to 36 floats
+    static constexpr int kStgRow = 36;
+    static constexpr int kStgOff = kLOff + kStages * 2 * kT * 4;
+    static constexpr int kBarOff = kStgOff + 4 * 32 * kStgRow * 4;
     // kv_full, q_full[S], q_empty[S], s_full, ds_ready, it_done, dq_free, drain
     static constexpr int kNumBars = 6 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS = 0;
     static constexpr uint32_t kColDP = 128;
@@ -123,6 +128,13 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
                  "f"(d)
                  : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
+    float4 x;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w) : "r"(addr)
+                 : "memory");
+    return x;
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -198,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             mbar_init(bar_qe(s), 1);
         }
         mbar_init(bar_s, 1);
-        mbar_init(bar_ds, 128);
+        mbar_init(bar_ds, 256);
         mbar_init(bar_it, 1);
         mbar_init(bar_dqf, 128);
         mbar_init(bar_drain, 1);
@@ -276,12 +288,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             constexpr uint32_t id_s = idesc_f16_f32(kT, kT, 0, 0);      // S^T, dP^T
             constexpr uint32_t id_kv = idesc_f16_f32(kT, D, 0, 1);      // dV, dK (B MN-major)
             constexpr uint32_t id_q = idesc_f16_f32(kT, D, 1, 1);       // dQ (A and B MN-major)
+            // Descriptors of every operand tile at offset 0, K-major (_k) and
+            // MN-major (_mn) views; a stage or K step adds its byte offset >> 4
+            // to the start-address field (the issuing thread's per-MMA work
+            // is what bounds how fast the MMAs can be fed).
+            const uint64_t k_k = smem_desc_sw128(sK, 16, 1024), k_mn = smem_desc_sw128(sK, C::kChunkBytes, 1024);
+            const uint64_t v_k = smem_desc_sw128(sV, 16, 1024);
+            const uint64_t q_k = smem_desc_sw128(sQ, 16, 1024), q_mn = smem_desc_sw128(sQ, C::kChunkBytes, 1024);
+            const uint64_t o_k = smem_desc_sw128(sO, 16, 1024), o_mn = smem_desc_sw128(sO, C::kChunkBytes, 1024);
+            const uint64_t ds_k[2] = {smem_desc_sw128(sS, 16, 1024), smem_desc_sw128(sS2, 16, 1024)};
+            const uint64_t ds_mn[2] = {smem_desc_sw128(sS, C::kChunkBytes, 1024),
+                                       smem_desc_sw128(sS2, C::kChunkBytes, 1024)};
+            // K step kk of a K-major tile (two 64-column chunks) / of an MN-major tile (16 rows)
+            auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4); };
+            auto moff = [](int kk) { return (uint64_t)(kk * (2048 >> 4)); };
+            // TMEM column of P^T (P_lo) for K step kk: query columns 0-63 are
+            // packed into columns 0-31, 64-127 into 64-95 (one softmax group each)
+            auto pk = [](int kk) { return (uint32_t)(kk * 8 + (kk >> 2) * 32); };
             bool ok = mbar_wait(bar_kv, 0, abort_flag);
             tc_fence_after();
             int i = 0;
             ring_walk_q(p.tab, kt.shard, [&](int, int nq, int natq) {
                 if (!ok || !active(nq, natq)) return;
                 const int s = i % C::kStages;
+                const uint64_t st = (uint64_t)(s * (C::kTileBytes >> 4));
                 // S^T(i) overwrites P^T(i-1) and dP^T(i) overwrites P_lo(i-1),
                 // both read by MMAs of iteration i-1 issued earlier (the
                 // tcgen05.mma operations of one thread run in issue order); the
@@ -289,24 +319,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 ok = mbar_wait(bar_qf(s), (i / C::kStages) & 1, abort_flag);
                 if (!ok) return;
                 tc_fence_after();
-                const uint32_t q_t = sQ + s * C::kTileBytes, o_t = sO + s * C::kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::kColS, smem_desc_sw128(sK + off, 16, 1024),
-                           smem_desc_sw128(q_t + off, 16, 1024), id_s, kk > 0);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::kColS, k_k + koff(kk), q_k + st + koff(kk), id_s, kk > 0);
                 if (i > 0) {
                     ok = mbar_wait(bar_dqf, (i - 1) & 1, abort_flag);
                     if (!ok) return;
                     tc_fence_after();
                 }
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::kColDP, smem_desc_sw128(sV + off, 16, 1024),
-                           smem_desc_sw128(o_t + off, 16, 1024), id_s, kk > 0);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::kColDP, v_k + koff(kk), o_k + st + koff(kk), id_s, kk > 0);
                 mma_commit(bar_s);
                 ok = mbar_wait(bar_ds, i & 1, abort_flag);
                 if (!ok) return;
@@ -320,25 +343,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 // dV += P^T dO  (A: P^T fp16 in TMEM; B: dO, K = query rows, N = D)
 #pragma unroll
                 for (int kk = 0; kk < kT / 16; ++kk)
-                    mma_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
-                           smem_desc_sw128(o_t + kk * 2048, C::kChunkBytes, 1024), id_kv,
+                    mma_ts(tmem + C::kColDV, tmem + C::kColS + pk(kk), o_mn + st + moff(kk), id_kv,
                            (!seg_start(i) || kk > 0) ? 1u : 0u);
                 if (split) {
 #pragma unroll
                     for (int kk = 0; kk < kT / 16; ++kk)
-                        mma_ts(tmem + C::kColDV, tmem + C::kColDP + kk * 8,
-                               smem_desc_sw128(o_t + kk * 2048, C::kChunkBytes, 1024), id_kv, 1u);
+                        mma_ts(tmem + C::kColDV, tmem + C::kColDP + pk(kk), o_mn + st + moff(kk), id_kv, 1u);
                 }
                 // dK += dS^T Q  (A: dS^T K-major in smem; B: Q, K = query rows, N = D)
                 for (int part = 0; part < (split ? 2 : 1); ++part) {
-                    const uint32_t a_t = part == 0 ? sS : sS2;
 #pragma unroll
-                    for (int kk = 0; kk < kT / 16; ++kk) {
-                        const uint32_t aoff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                        mma_ss(tmem + C::kColDK, smem_desc_sw128(a_t + aoff, 16, 1024),
-                               smem_desc_sw128(q_t + kk * 2048, C::kChunkBytes, 1024), id_kv,
+                    for (int kk = 0; kk < kT / 16; ++kk)
+                        mma_ss(tmem + C::kColDK, ds_k[part] + koff(kk), q_mn + st + moff(kk), id_kv,
                                (!seg_start(i) || kk > 0 || part > 0) ? 1u : 0u);
-                    }
                 }
                 // Q(i) and dO(i) are read by no later MMA: the producer may refill
                 // the stage while dQ_t runs.
@@ -347,11 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 // It overwrites the P_lo columns, which the dV MMA above read
                 // first (tcgen05.mma operations of one thread run in order).
                 for (int part = 0; part < (split ? 2 : 1); ++part) {
-                    const uint32_t a_t = part == 0 ? sS : sS2;
 #pragma unroll
                     for (int kk = 0; kk < kT / 16; ++kk)
-                        mma_ss(tmem + C::kColDP, smem_desc_sw128(a_t + kk * 2048, C::kChunkBytes, 1024),
-                               smem_desc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), id_q,
+                        mma_ss(tmem + C::kColDP, ds_mn[part] + moff(kk), k_mn + moff(kk), id_q,
                                (kk > 0 || part > 0) ? 1u : 0u);
                 }
                 mma_commit(bar_it);
@@ -360,19 +375,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             mma_commit(bar_drain);
             mbar_wait_drain(bar_drain, 0);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ------------------------------------------------ softmax (one key row per thread)
+    } else if (warp >= 4) {
+        // ------------------------------------------------ softmax, dQ reduction, epilogue
+        // Two groups of four warps, one key row per thread in each: group 0
+        // (warps 4-7) forms P^T and dS^T for query columns 0-63 and writes
+        // dV; group 1 (warps 8-11) does query columns 64-127, writes dK, and
+        // drains dQ_t (one query row per thread) after each tile's MMAs.
+        const int grp = (warp - 4) >> 2;
         const int quad = warp & 3;
-        const int r = quad * 32 + lane;               // key row within the tile
+        const int r = quad * 32 + lane;               // key row (softmax) / query row (dQ drain)
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         const int natk = kt.nat0 + r;
         const float sl2 = ldexpf(p.scale_log2, p.exps[0] + p.exps[1]);    // S' -> scaled log2 units
-        // Write (or, after a flush, add) this key row's dV and scale * dK from
-        // the TMEM accumulators into the outputs.
+        const float sc = ldexpf(p.scale, p.exps[4] + p.exps[1]);           // dQ_t -> dQ
+        const uint32_t stg = sbase + C::kStgOff + (uint32_t)(quad * 32 * C::kStgRow * 4);   // dQ staging rows
+        // Write (or, after a flush, add) this key row's dV (group 0) or
+        // scale * dK (group 1) from the TMEM accumulator into the output.
         auto emit = [&](bool have, bool add) {
             const int64_t off = (((int64_t)b * S + kt.row0 + r) * H + h) * D;
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
+            {
+                const int which = grp;
                 const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
                 const float mul = which == 0 ? ldexpf(1.f, p.exps[3] - kPShift)
                                              : ldexpf(p.scale, p.exps[4] + p.exps[0]);
@@ -426,12 +448,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // causal diagonal and ragged key tiles need a per-element mask; query
         // columns past the tile end are zeroed by their -inf statistic) and
         // kLo (hi + lo fp16 parts of P and dS, see the MMA issuer).
+        // TMEM column of the packed P^T (or P_lo) for 32-column chunk c4
+        auto pcol = [](int c4) { return (uint32_t)(c4 * 16 + (c4 >> 1) * 32); };
         auto tile_pass = [&](auto mask_tag, auto lo_tag, const float* ls, int cmin) {
             constexpr bool kMask = decltype(mask_tag)::value;
             constexpr bool kLo = decltype(lo_tag)::value;
             const bool row_ok = r < kt.nq;
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c4 = 2 * grp + cc;   // this group's 32-column chunks
                 uint32_t sv[32], dv[32];
                 tmem_ld32(lane_base + C::kColS + c4 * 32, sv);
                 tmem_ld32(lane_base + C::kColDP + c4 * 32, dv);
@@ -472,9 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                         }
                     }
                 }
-                // P^T chunk -> S columns already read; P_lo -> dP^T columns already read
-                tmem_st16(lane_base + C::kColS + c4 * 16, pp);
-                if constexpr (kLo) tmem_st16(lane_base + C::kColDP + c4 * 16, pl);
+                // P^T chunk -> S columns this group has already read (query
+                // columns 0-63 -> columns 0-31, 64-127 -> 64-95); P_lo likewise
+                // into the dP^T columns
+                tmem_st16(lane_base + C::kColS + pcol(c4), pp);
+                if constexpr (kLo) tmem_st16(lane_base + C::kColDP + pcol(c4), pl);
                 // dS^T columns c4*32 .. +31 = 16-byte units 4*(c4&1) .. +3 of chunk c4>>1
                 const uint32_t coff = (uint32_t)r * 128 + (uint32_t)(c4 >> 1) * C::kChunkBytes;
 #pragma unroll
@@ -487,13 +514,53 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 }
             }
         };
+        // dQ_t of the tile whose MMAs just finished -> dq_acc (group 1)
+        auto drain = [&](int q0, int nq) {
+            // The whole row of dQ_t comes into registers first and the TMEM
+            // columns are released at once: the next dP^T waits for this
+            // signal, and the reductions below then overlap its MMAs.
+            uint32_t v[D];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c)
+                tmem_ld32(lane_base + C::kColDP + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar_dqf);
+            // Reductions in coalesced form: per 32-column chunk the warp's 32
+            // rows go through shared memory, and each red.v4 instruction then
+            // covers 4 rows x 128 contiguous bytes instead of 32 rows x 16
+            // bytes (32 separate transactions).  Rows are padded to 36 floats:
+            // both the row-wise writes and the transposed reads are free of
+            // bank conflicts.
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    st_shared_v4(stg + (uint32_t)((lane * C::kStgRow + 4 * k) * 4),
+                                 __float_as_uint(__uint_as_float(v[c * 32 + 4 * k]) * sc),
+                                 __float_as_uint(__uint_as_float(v[c * 32 + 4 * k + 1]) * sc),
+                                 __float_as_uint(__uint_as_float(v[c * 32 + 4 * k + 2]) * sc),
+                                 __float_as_uint(__uint_as_float(v[c * 32 + 4 * k + 3]) * sc));
+                __syncwarp();
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int rr = 4 * it + (lane >> 3), col = (lane & 7) * 4;
+                    const float4 x = ld_shared_v4f(stg + (uint32_t)((rr * C::kStgRow + col) * 4));
+                    if (quad * 32 + rr < nq)
+                        red_add_v4(p.dq_acc + (((int64_t)b * S + q0 + quad * 32 + rr) * H + h) * D + c * 32 + col,
+                                   x.x, x.y, x.z, x.w);
+                }
+                __syncwarp();
+            }
+        };
         int i = 0;
         bool ok = true;
-        ring_walk_q(p.tab, kt.shard, [&](int, int nq, int natq) {
+        ring_walk_q(p.tab, kt.shard, [&](int q0, int nq, int natq) {
             if (!ok || !active(nq, natq)) return;
             if (flush_tile && i > 0 && (i % kFlush) == 0) {
-                // promote the finished segment (all MMAs of iteration i-1 done)
-                ok = __all_sync(0xffffffffu, mbar_wait(bar_it, (i - 1) & 1, abort_flag));
+                // promote the finished segment (all MMAs of iteration i-1 done;
+                // group 1 waited for them in its drain)
+                if (grp == 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_it, (i - 1) & 1, abort_flag));
                 if (!ok) return;
                 tc_fence_after();
                 emit(true, flushed);
@@ -519,45 +586,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             fence_proxy_async();
             tc_fence_before();
             mbar_arrive(bar_ds);
+            if (grp == 1) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar_it, i & 1, abort_flag));
+                if (!ok) return;
+                tc_fence_after();
+                drain(q0, nq);
+            }
             ++i;
         });
-        // epilogue: dV and scale * dK for this key row
-        if (ok && i > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_it, (i - 1) & 1, abort_flag));
+        // epilogue: dV (group 0) or scale * dK (group 1) for this key row;
+        // group 1 waited for the last tile's MMAs in its drain
+        if (ok && i > 0 && grp == 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_it, (i - 1) & 1, abort_flag));
         if (ok) {
             tc_fence_after();
             emit(i > 0, flushed);
         }
-    } else if (warp >= 8) {
-        // ------------------------------------------------ dQ reduction (one query row per thread)
-        const int quad = warp & 3;
-        const int r = quad * 32 + lane;
-        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        const float sc = ldexpf(p.scale, p.exps[4] + p.exps[1]);
-        int i = 0;
-        bool ok = true;
-        ring_walk_q(p.tab, kt.shard, [&](int q0, int nq, int natq) {
-            if (!ok || !active(nq, natq)) return;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_it, i & 1, abort_flag));
-            if (!ok) return;
-            tc_fence_after();
-            float* dst = p.dq_acc + (((int64_t)b * S + q0 + r) * H + h) * D;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(lane_base + C::kColDP + c * 32, v);
-                tmem_wait_ld();
-                if (r < nq) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        red_add_v4(dst + c * 32 + 4 * e, __uint_as_float(v[4 * e]) * sc,
-                                   __uint_as_float(v[4 * e + 1]) * sc, __uint_as_float(v[4 * e + 2]) * sc,
-                                   __uint_as_float(v[4 * e + 3]) * sc);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(bar_dqf);
-            ++i;
-        });
     }
 
     tc_fence_before();
