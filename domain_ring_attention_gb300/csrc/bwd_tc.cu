@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // kLo (hi + lo fp16 parts of P and dS, see the MMA issuer).
         // TMEM column of the packed P^T (or P_lo) for 32-column chunk c4
         auto pcol = [](int c4) { return (uint32_t)(c4 * 16 + (c4 >> 1) * 32); };
-        auto tile_pass = [&](auto mask_tag, auto lo_tag, const float* ls, int cmin) {
+        auto tile_pass = [&](auto mask_tag, auto lo_tag, uint32_t ls, int cmin) {
             constexpr bool kMask = decltype(mask_tag)::value;
             constexpr bool kLo = decltype(lo_tag)::value;
             const bool row_ok = r < kt.nq;
@@ -466,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 for (int e2 = 0; e2 < 8; ++e2) {
                     // statistics of columns c .. c+3 (broadcast shared loads)
                     const int c = c4 * 32 + 4 * e2;
-                    const float4 nl = *reinterpret_cast<const float4*>(ls + c);
-                    const float4 nd = *reinterpret_cast<const float4*>(ls + kT + c);
+                    const float4 nl = ld_shared_v4f(ls + (uint32_t)(c * 4));
+                    const float4 nd = ld_shared_v4f(ls + (uint32_t)((kT + c) * 4));
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const int e = 2 * e2 + h2;
@@ -571,7 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_s, i & 1, abort_flag));
             if (!ok) return;
             tc_fence_after();
-            const float* ls = lse_s + s * 2 * kT;
+            // this stage's row statistics (shared-memory address)
+            const uint32_t ls = sbase + C::kLOff + (uint32_t)(s * 2 * kT * 4);
             const int kind = classify(causal, natq, nq, kt.nat0, kt.nq, kT);
             if (kind == kPartial) {
                 // causal: query column c sees key natk iff natk <= natq + c
