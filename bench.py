@@ -37,10 +37,12 @@ from domain_ring_attention_gb300.workloads import WORKLOADS, make_inputs
 METRIC = "ring-attention fwd/bwd TFLOP/s (bf16, S=65536) and % of GB300 dense-BF16 peak"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
-# dram bytes (read + write) per launch of the forward kernel from the committed
-# ncu capture of the current kernel version; None when not captured for it.
-NCU_TRAFFIC_BYTES = {}
-KERNEL_VERSION = "fwd_tc_v1"
+# dram bytes (read + write) per launch of the forward kernel on the default
+# workload, from the committed ncu capture of the kernel version named here
+# (2-head capture scaled by 8 to 16 heads: the traffic is per head); a kernel
+# change without a new capture must drop its entry (traffic is then null).
+NCU_TRAFFIC_BYTES = {"fwd_tc@4218d0c": 8 * (50.380544e6 + 1.218048e6)}
+KERNEL_VERSION = "fwd_tc@4218d0c"
 
 
 def parse():
