@@ -20,9 +20,9 @@
 //
 // Warp roles (384 threads): warp 0 TMA producer (+ lse / Delta staging),
 // warp 1 TMEM allocator + MMA issuer, warps 4-7 softmax for query columns
-// 0-63 (one key row per thread) and the dV epilogue, warps 8-11 softmax for
-// columns 64-127, the dK epilogue and the dQ reduction (one query row per
-// thread).  Tensor memory: S^T|P^T, dP^T|dQ_t, dV, dK.  Every barrier
+// 0-63 (one key row per thread), half of the dQ reduction (one query row per
+// thread) and the dV epilogue, warps 8-11 the same for columns 64-127 and the
+// dK epilogue.  Tensor memory: S^T|P^T, dP^T|dQ_t, dV, dK.  Every barrier
 // wait is bounded (tc_ptx.cuh).
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -60,10 +60,10 @@ struct Cfg {
     static constexpr int kSOff = kOOff + kStages * kTileBytes;     // dS^T (hi), 128 x 128 fp16
     static constexpr int kS2Off = kSOff + 2 * kChunkBytes;         // dS^T lo part (partial tiles)
     static constexpr int kLOff = kS2Off + 2 * kChunkBytes;         // [stage] lse*log2e, Delta
-    // dQ staging: per reducer warp 32 rows x 32 fp32, rows padded to 36 floats
-    static constexpr int kStgRow = 36;
+    // dQ staging: per softmax warp (8) 32 rows x 16 fp32, rows padded to 20 floats
+    static constexpr int kStgRow = 20;
     static constexpr int kStgOff = kLOff + kStages * 2 * kT * 4;
-    static constexpr int kBarOff = kStgOff + 4 * 32 * kStgRow * 4;
+    static constexpr int kBarOff = kStgOff + 8 * 32 * kStgRow * 4;
     // kv_full, q_full[S], q_empty[S], s_full, ds_ready, it_done, dq_free, drain
     static constexpr int kNumBars = 6 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(bar_s, 1);
         mbar_init(bar_ds, 256);
         mbar_init(bar_it, 1);
-        mbar_init(bar_dqf, 128);
+        mbar_init(bar_dqf, 256);
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const int natk = kt.nat0 + r;
         const float sl2 = ldexpf(p.scale_log2, p.exps[0] + p.exps[1]);    // S' -> scaled log2 units
         const float sc = ldexpf(p.scale, p.exps[4] + p.exps[1]);           // dQ_t -> dQ
-        const uint32_t stg = sbase + C::kStgOff + (uint32_t)(quad * 32 * C::kStgRow * 4);   // dQ staging rows
+        const uint32_t stg = sbase + C::kStgOff + (uint32_t)((grp * 4 + quad) * 32 * C::kStgRow * 4);   // dQ staging
         // Write (or, after a flush, add) this key row's dV (group 0) or
         // scale * dK (group 1) from the TMEM accumulator into the output.
         auto emit = [&](bool have, bool add) {
@@ -515,39 +515,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             }
         };
         // dQ_t of the tile whose MMAs just finished -> dq_acc (group 1)
+        // dQ_t of the tile whose MMAs just finished -> dq_acc; each group
+        // takes half of the columns (one query row per thread)
         auto drain = [&](int q0, int nq) {
-            // The whole row of dQ_t comes into registers first and the TMEM
-            // columns are released at once: the next dP^T waits for this
-            // signal, and the reductions below then overlap its MMAs.
-            uint32_t v[D];
+            // This group's columns of the row come into registers first and
+            // the TMEM is released at once (the next dP^T waits for both
+            // groups); the reductions then overlap that MMA.
+            constexpr int kCols = D / 2;
+            uint32_t v[kCols];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c)
-                tmem_ld32(lane_base + C::kColDP + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+            for (int c = 0; c < kCols / 32; ++c)
+                tmem_ld32(lane_base + C::kColDP + grp * kCols + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar_dqf);
-            // Reductions in coalesced form: per 32-column chunk the warp's 32
+            // Reductions in coalesced form: per 16-column chunk the warp's 32
             // rows go through shared memory, and each red.v4 instruction then
-            // covers 4 rows x 128 contiguous bytes instead of 32 rows x 16
-            // bytes (32 separate transactions).  Rows are padded to 36 floats:
-            // both the row-wise writes and the transposed reads are free of
-            // bank conflicts.
+            // covers 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes
+            // (32 separate transactions).  Rows padded to 20 floats keep the
+            // row-wise writes and the transposed reads free of bank conflicts.
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < kCols / 16; ++c) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
+                for (int k = 0; k < 4; ++k)
                     st_shared_v4(stg + (uint32_t)((lane * C::kStgRow + 4 * k) * 4),
-                                 __float_as_uint(__uint_as_float(v[c * 32 + 4 * k]) * sc),
-                                 __float_as_uint(__uint_as_float(v[c * 32 + 4 * k + 1]) * sc),
-                                 __float_as_uint(__uint_as_float(v[c * 32 + 4 * k + 2]) * sc),
-                                 __float_as_uint(__uint_as_float(v[c * 32 + 4 * k + 3]) * sc));
+                                 __float_as_uint(__uint_as_float(v[c * 16 + 4 * k]) * sc),
+                                 __float_as_uint(__uint_as_float(v[c * 16 + 4 * k + 1]) * sc),
+                                 __float_as_uint(__uint_as_float(v[c * 16 + 4 * k + 2]) * sc),
+                                 __float_as_uint(__uint_as_float(v[c * 16 + 4 * k + 3]) * sc));
                 __syncwarp();
 #pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    const int rr = 4 * it + (lane >> 3), col = (lane & 7) * 4;
+                for (int it = 0; it < 4; ++it) {
+                    const int rr = 8 * it + (lane >> 2), col = (lane & 3) * 4;
                     const float4 x = ld_shared_v4f(stg + (uint32_t)((rr * C::kStgRow + col) * 4));
                     if (quad * 32 + rr < nq)
-                        red_add_v4(p.dq_acc + (((int64_t)b * S + q0 + quad * 32 + rr) * H + h) * D + c * 32 + col,
+                        red_add_v4(p.dq_acc + (((int64_t)b * S + q0 + quad * 32 + rr) * H + h) * D + grp * kCols +
+                                       c * 16 + col,
                                    x.x, x.y, x.z, x.w);
                 }
                 __syncwarp();
@@ -558,10 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         ring_walk_q(p.tab, kt.shard, [&](int q0, int nq, int natq) {
             if (!ok || !active(nq, natq)) return;
             if (flush_tile && i > 0 && (i % kFlush) == 0) {
-                // promote the finished segment (all MMAs of iteration i-1 done;
-                // group 1 waited for them in its drain)
-                if (grp == 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_it, (i - 1) & 1, abort_flag));
-                if (!ok) return;
+                // promote the finished segment (all MMAs of iteration i-1 done:
+                // waited for in the drain)
                 tc_fence_after();
                 emit(true, flushed);
                 flushed = true;
@@ -587,17 +588,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             fence_proxy_async();
             tc_fence_before();
             mbar_arrive(bar_ds);
-            if (grp == 1) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar_it, i & 1, abort_flag));
-                if (!ok) return;
-                tc_fence_after();
-                drain(q0, nq);
-            }
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_it, i & 1, abort_flag));
+            if (!ok) return;
+            tc_fence_after();
+            drain(q0, nq);
             ++i;
         });
-        // epilogue: dV (group 0) or scale * dK (group 1) for this key row;
-        // group 1 waited for the last tile's MMAs in its drain
-        if (ok && i > 0 && grp == 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_it, (i - 1) & 1, abort_flag));
+        // epilogue: dV (group 0) or scale * dK (group 1) for this key row (the
+        // last tile's MMAs were waited for in its drain)
         if (ok) {
             tc_fence_after();
             emit(i > 0, flushed);
