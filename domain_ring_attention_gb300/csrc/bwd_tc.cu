@@ -16,7 +16,7 @@
 //   dV  += P^T dO           (A = P^T from TMEM)
 //   dK  += dS^T Q           (A = dS^T, K-major view of the smem tile)
 //   dQ_t = dS K             (A = dS, MN-major view of the same smem tile)
-//   dQ  += scale dQ_t       (reduction warps: TMEM -> red.global.add.v4.f32)
+//   dQ  += scale dQ_t       (softmax warps: TMEM -> shared memory -> TMA bulk reduction)
 //
 // Warp roles (384 threads): warp 0 TMA producer (+ lse / Delta staging),
 // warp 1 TMEM allocator + MMA issuer, warps 4-7 softmax for query columns
@@ -60,10 +60,11 @@ struct Cfg {
     static constexpr int kSOff = kOOff + kStages * kTileBytes;     // dS^T (hi), 128 x 128 fp16
     static constexpr int kS2Off = kSOff + 2 * kChunkBytes;         // dS^T lo part (partial tiles)
     static constexpr int kLOff = kS2Off + 2 * kChunkBytes;         // [stage] lse*log2e, Delta
-    // dQ staging: per softmax warp (8) 32 rows x 16 fp32, rows padded to 20 floats
-    static constexpr int kStgRow = 20;
-    static constexpr int kStgOff = kLOff + kStages * 2 * kT * 4;
-    static constexpr int kBarOff = kStgOff + 8 * 32 * kStgRow * 4;
+    // dQ staging for the TMA reductions: per softmax warp (8) two buffers of
+    // 32 rows x 16 fp32 (2 KB, 64-byte swizzle)
+    static constexpr int kStgBytes = 32 * 16 * 4;
+    static constexpr int kStgOff = (kLOff + kStages * 2 * kT * 4 + 1023) / 1024 * 1024;
+    static constexpr int kBarOff = kStgOff + 8 * 2 * kStgBytes;
     // kv_full, q_full[S], q_empty[S], s_full, ds_ready, it_done, dq_free, drain
     static constexpr int kNumBars = 6 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -88,6 +89,7 @@ struct BwdParams {
     CUtensorMap tk;
     CUtensorMap tv;
     CUtensorMap tdo;
+    CUtensorMap tdq;          // dq_acc, fp32, box 16 x 32 rows, 64-byte swizzle
     SegTable tab;             // 128-row tiles
     const float* lse;         // [B,H,S]
     const float* delta;       // [B,H,S]
@@ -122,12 +124,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
-                 : "memory");
 }
 
 __device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
@@ -388,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const int natk = kt.nat0 + r;
         const float sl2 = ldexpf(p.scale_log2, p.exps[0] + p.exps[1]);    // S' -> scaled log2 units
         const float sc = ldexpf(p.scale, p.exps[4] + p.exps[1]);           // dQ_t -> dQ
-        const uint32_t stg = sbase + C::kStgOff + (uint32_t)((grp * 4 + quad) * 32 * C::kStgRow * 4);   // dQ staging
+        const uint32_t stg = sbase + C::kStgOff + (uint32_t)((grp * 4 + quad) * 2 * C::kStgBytes);   // dQ staging
         // Write (or, after a flush, add) this key row's dV (group 0) or
         // scale * dK (group 1) from the TMEM accumulator into the output.
         auto emit = [&](bool have, bool add) {
@@ -529,31 +525,36 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar_dqf);
-            // Reductions in coalesced form: per 16-column chunk the warp's 32
-            // rows go through shared memory, and each red.v4 instruction then
-            // covers 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes
-            // (32 separate transactions).  Rows padded to 20 floats keep the
-            // row-wise writes and the transposed reads free of bank conflicts.
+            // The reductions go through the TMA: per 16-column chunk the warp
+            // writes its 32 rows into a shared-memory tile (rows past the query
+            // tile as zeros, which add nothing) and one lane issues a bulk
+            // tensor reduction (add) into dq_acc, so L2 reduces whole lines
+            // instead of one 16-byte atomic per thread and chunk.  Two buffers
+            // per warp: a buffer is rewritten once the reduction issued two
+            // chunks ago has read it.
+            const bool row_ok = quad * 32 + lane < nq;
 #pragma unroll
             for (int c = 0; c < kCols / 16; ++c) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    st_shared_v4(stg + (uint32_t)((lane * C::kStgRow + 4 * k) * 4),
-                                 __float_as_uint(__uint_as_float(v[c * 16 + 4 * k]) * sc),
-                                 __float_as_uint(__uint_as_float(v[c * 16 + 4 * k + 1]) * sc),
-                                 __float_as_uint(__uint_as_float(v[c * 16 + 4 * k + 2]) * sc),
-                                 __float_as_uint(__uint_as_float(v[c * 16 + 4 * k + 3]) * sc));
+                const uint32_t buf = stg + (uint32_t)((c & 1) * C::kStgBytes);
+                if (lane == 0) bulk_wait_read_1();
                 __syncwarp();
 #pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    const int rr = 8 * it + (lane >> 2), col = (lane & 3) * 4;
-                    const float4 x = ld_shared_v4f(stg + (uint32_t)((rr * C::kStgRow + col) * 4));
-                    if (quad * 32 + rr < nq)
-                        red_add_v4(p.dq_acc + (((int64_t)b * S + q0 + quad * 32 + rr) * H + h) * D + grp * kCols +
-                                       c * 16 + col,
-                                   x.x, x.y, x.z, x.w);
+                for (int k = 0; k < 4; ++k) {
+                    // 16-byte unit k of row `lane` under the 64-byte swizzle
+                    const uint32_t unit = (uint32_t)(k ^ ((lane >> 1) & 3));
+                    const int e = c * 16 + 4 * k;
+                    st_shared_v4(buf + (uint32_t)(lane * 64) + unit * 16,
+                                 row_ok ? __float_as_uint(__uint_as_float(v[e]) * sc) : 0u,
+                                 row_ok ? __float_as_uint(__uint_as_float(v[e + 1]) * sc) : 0u,
+                                 row_ok ? __float_as_uint(__uint_as_float(v[e + 2]) * sc) : 0u,
+                                 row_ok ? __float_as_uint(__uint_as_float(v[e + 3]) * sc) : 0u);
                 }
+                fence_proxy_async();
                 __syncwarp();
+                if (lane == 0) {
+                    tma_reduce_add_4d(&p.tdq, buf, grp * kCols + c * 16, h, q0 + quad * 32, b);
+                    bulk_commit_group();
+                }
             }
         };
         int i = 0;
@@ -600,6 +601,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             tc_fence_after();
             emit(i > 0, flushed);
         }
+        // the staged dQ reductions have completed before the CTA exits
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -633,6 +637,20 @@ EncodeTiledFn get_encode() {
 }
 
 // BSHD fp16 tensor as a 4-D map (d, H, S, B), box (64, 1, 128, 1), 128-byte swizzle.
+// dq_acc (fp32 [B,S,H,d]) as a 4-D map (d, H, S, B), box (16, 1, 32, 1), 64-byte
+// swizzle: the tile one dQ-reducing warp adds per chunk.
+bool make_map_dq(CUtensorMap* m, void* base, int B, int S, int H, int d) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4, (cuuint64_t)S * H * d * 4};
+    const cuuint32_t box[4] = {16, 1, 32, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int d) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return false;
@@ -651,7 +669,8 @@ int launch_t(const st_layout& L, const BwdArgs& a, void* stream) {
     BwdParams p;
     const int S = (int)L.S;
     if (!make_map(&p.tq, a.h16[0], a.B, S, a.H, D) || !make_map(&p.tk, a.h16[1], a.B, S, a.H, D) ||
-        !make_map(&p.tv, a.h16[2], a.B, S, a.H, D) || !make_map(&p.tdo, a.h16[3], a.B, S, a.H, D))
+        !make_map(&p.tv, a.h16[2], a.B, S, a.H, D) || !make_map(&p.tdo, a.h16[3], a.B, S, a.H, D) ||
+        !make_map_dq(&p.tdq, a.dq_acc, a.B, S, a.H, D))
         return (int)cudaErrorInvalidValue;
     fill_segtable(L, kT, &p.tab);
     // Longest-processing-time-first order for causal work: a key tile starting
