@@ -60,11 +60,7 @@ struct Cfg {
     static constexpr int kSOff = kOOff + kStages * kTileBytes;     // dS^T (hi), 128 x 128 fp16
     static constexpr int kS2Off = kSOff + 2 * kChunkBytes;         // dS^T lo part (partial tiles)
     static constexpr int kLOff = kS2Off + 2 * kChunkBytes;         // [stage] lse*log2e, Delta
-    // dQ staging for the TMA reductions: per softmax warp (8) two buffers of
-    // 32 rows x 16 fp32 (2 KB, 64-byte swizzle)
-    static constexpr int kStgBytes = 32 * 16 * 4;
-    static constexpr int kStgOff = (kLOff + kStages * 2 * kT * 4 + 1023) / 1024 * 1024;
-    static constexpr int kBarOff = kStgOff + 8 * 2 * kStgBytes;
+    static constexpr int kBarOff = kLOff + kStages * 2 * kT * 4;
     // kv_full, q_full[S], q_empty[S], s_full, ds_ready, it_done, dq_free, drain
     static constexpr int kNumBars = 6 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -89,7 +85,7 @@ struct BwdParams {
     CUtensorMap tk;
     CUtensorMap tv;
     CUtensorMap tdo;
-    CUtensorMap tdq;          // dq_acc, fp32, box 16 x 32 rows, 64-byte swizzle
+    CUtensorMap tdq;          // dq_acc, fp32, box 32 x 32 rows, 128-byte swizzle
     SegTable tab;             // 128-row tiles
     const float* lse;         // [B,H,S]
     const float* delta;       // [B,H,S]
@@ -384,7 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const int natk = kt.nat0 + r;
         const float sl2 = ldexpf(p.scale_log2, p.exps[0] + p.exps[1]);    // S' -> scaled log2 units
         const float sc = ldexpf(p.scale, p.exps[4] + p.exps[1]);           // dQ_t -> dQ
-        const uint32_t stg = sbase + C::kStgOff + (uint32_t)((grp * 4 + quad) * 2 * C::kStgBytes);   // dQ staging
+        // dQ staging: the 4 KB of the dS^T tile (and of its lo part) that this
+        // warp itself writes -- its 32 key rows of its group's 64 columns -- are
+        // free from the end of a tile's MMAs until its next softmax pass
+        const uint32_t stg0 = sS + (uint32_t)(grp * C::kChunkBytes + quad * 32 * 128);
+        const uint32_t stg1 = sS2 + (uint32_t)(grp * C::kChunkBytes + quad * 32 * 128);
         // Write (or, after a flush, add) this key row's dV (group 0) or
         // scale * dK (group 1) from the TMEM accumulator into the output.
         auto emit = [&](bool have, bool add) {
@@ -525,25 +525,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar_dqf);
-            // The reductions go through the TMA: per 16-column chunk the warp
-            // writes its 32 rows into a shared-memory tile (rows past the query
-            // tile as zeros, which add nothing) and one lane issues a bulk
-            // tensor reduction (add) into dq_acc, so L2 reduces whole lines
-            // instead of one 16-byte atomic per thread and chunk.  Two buffers
-            // per warp: a buffer is rewritten once the reduction issued two
-            // chunks ago has read it.
+            // The reductions go through the TMA: per 32-column chunk the warp
+            // writes its 32 rows into a 128-byte-swizzled fp32 tile (rows past
+            // the query tile as zeros, which add nothing) and one lane issues a
+            // bulk tensor reduction (add) into dq_acc; the warp then goes on to
+            // its next softmax pass while the reductions run.
             const bool row_ok = quad * 32 + lane < nq;
 #pragma unroll
-            for (int c = 0; c < kCols / 16; ++c) {
-                const uint32_t buf = stg + (uint32_t)((c & 1) * C::kStgBytes);
-                if (lane == 0) bulk_wait_read_1();
-                __syncwarp();
+            for (int c = 0; c < kCols / 32; ++c) {
+                const uint32_t buf = c == 0 ? stg0 : stg1;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    // 16-byte unit k of row `lane` under the 64-byte swizzle
-                    const uint32_t unit = (uint32_t)(k ^ ((lane >> 1) & 3));
-                    const int e = c * 16 + 4 * k;
-                    st_shared_v4(buf + (uint32_t)(lane * 64) + unit * 16,
+                for (int k = 0; k < 8; ++k) {
+                    // 16-byte unit k of row `lane` under the 128-byte swizzle
+                    const uint32_t unit = (uint32_t)(k ^ (lane & 7));
+                    const int e = c * 32 + 4 * k;
+                    st_shared_v4(buf + (uint32_t)(lane * 128) + unit * 16,
                                  row_ok ? __float_as_uint(__uint_as_float(v[e]) * sc) : 0u,
                                  row_ok ? __float_as_uint(__uint_as_float(v[e + 1]) * sc) : 0u,
                                  row_ok ? __float_as_uint(__uint_as_float(v[e + 2]) * sc) : 0u,
@@ -551,11 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 }
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) {
-                    tma_reduce_add_4d(&p.tdq, buf, grp * kCols + c * 16, h, q0 + quad * 32, b);
-                    bulk_commit_group();
-                }
+                if (lane == 0) tma_reduce_add_4d(&p.tdq, buf, grp * kCols + c * 32, h, q0 + quad * 32, b);
             }
+            if (lane == 0) bulk_commit_group();
         };
         int i = 0;
         bool ok = true;
@@ -573,6 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_s, i & 1, abort_flag));
             if (!ok) return;
             tc_fence_after();
+            // the dQ tiles staged in this warp's part of the dS^T buffers have
+            // been read by the TMA before the softmax pass overwrites them
+            if (lane == 0) bulk_wait_read_0();
+            __syncwarp();
             // this stage's row statistics (shared-memory address)
             const uint32_t ls = sbase + C::kLOff + (uint32_t)(s * 2 * kT * 4);
             const int kind = classify(causal, natq, nq, kt.nat0, kt.nq, kT);
@@ -637,17 +635,17 @@ EncodeTiledFn get_encode() {
 }
 
 // BSHD fp16 tensor as a 4-D map (d, H, S, B), box (64, 1, 128, 1), 128-byte swizzle.
-// dq_acc (fp32 [B,S,H,d]) as a 4-D map (d, H, S, B), box (16, 1, 32, 1), 64-byte
+// dq_acc (fp32 [B,S,H,d]) as a 4-D map (d, H, S, B), box (32, 1, 32, 1), 128-byte
 // swizzle: the tile one dQ-reducing warp adds per chunk.
 bool make_map_dq(CUtensorMap* m, void* base, int B, int S, int H, int d) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4, (cuuint64_t)S * H * d * 4};
-    const cuuint32_t box[4] = {16, 1, 32, 1};
+    const cuuint32_t box[4] = {32, 1, 32, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
