@@ -140,8 +140,10 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        if self.proc is None:
-            return None
+        """Median SM clock, its maximum and the throttle reasons seen (computed
+        once; later calls return the same result)."""
+        if getattr(self, "_summary", None) is not None or self.proc is None:
+            return getattr(self, "_summary", None)
         self.file.flush()
         rows = [l.strip().split(",") for l in open(self.file.name) if l.strip()]
         os.unlink(self.file.name)
@@ -158,8 +160,9 @@ class ClockSampler:
                 continue
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        self._summary = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                         "samples": len(sm)}
+        return self._summary
 
 
 def cpu_sample_tflops(wl, q, k, v, budget_s=12.0):
@@ -186,6 +189,44 @@ def cpu_sample_tflops(wl, q, k, v, budget_s=12.0):
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return flops / dt / 1e12, rows_done, dt, cores
+
+
+# ex2 results per clock per SM, measured on GB300 (ex2.approx.ftz.f32 throughput
+# probe: 30.5 per clock per SM with every warp issuing only exponentials)
+MUFU_EX2_PER_CLK_SM = 30.5
+GB300_SMS = 152
+
+
+def merge_gbs(st, wl, world, steps=10, warmup=3):
+    """Standalone log-sum-exp merge (st_attn_merge) of D per-KV-shard partials
+    of the workload's shape: HBM-bound, reported as algorithmic GB/s (partials
+    and their lse read once, out in bf16 and lse written once).  Inputs are
+    random partials (the merge's cost does not depend on their values) and far
+    larger than L2."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    po = torch.randn((wl.D, wl.B, wl.S, wl.H, wl.d), device=dev, dtype=torch.float32, generator=g)
+    pl = torch.randn((wl.D, wl.B, wl.H, wl.S), device=dev, dtype=torch.float32, generator=g)
+    out = torch.empty((wl.B, wl.S, wl.H, wl.d), device=dev, dtype=torch.bfloat16)
+    lse = torch.empty((wl.B, wl.H, wl.S), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        st.st_attn_merge(po, pl, out=out, lse=lse, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        st.st_attn_merge(po, pl, out=out, lse=lse, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    nbytes = po.numel() * 4 + pl.numel() * 4 + out.numel() * 2 + lse.numel() * 4
+    _, _, hbm, kind = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del po, pl
+    return {"kernel": "merge_kernel (st_attn_merge)", "D": wl.D, "bytes_per_launch": nbytes, "ms": ms,
+            "achieved_gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm, "peak_kind": kind + " HBM copy"}
 
 
 def train_step_tflops(st, world, steps=3, warmup=2):
@@ -322,6 +363,20 @@ def run_ours(args, rank, world):
     peak_b, peak_s, hbm, peak_kind = peaks()
     achieved = flops / (statistics.mean(launch_ms) * 1e-3) / 1e12
 
+    # exponentials: one per visible pair; against the MUFU rate measured on GB300
+    n_exp = wl.fwd_flops() / (4 * wl.d)
+    mufu = None
+    if not args.bwd:
+        clk_mhz = (clk.summary() or {}).get("sm_mhz") or 2070.0
+        peak_exp = MUFU_EX2_PER_CLK_SM * GB300_SMS * clk_mhz * 1e6
+        exps = n_exp / (statistics.mean(launch_ms) * 1e-3)
+        mufu = {"exps_per_s": exps, "peak_exps_per_s": peak_exp, "frac": exps / peak_exp,
+                "peak_kind": "measured ex2 throughput x 152 SMs x SM clock"}
+    merge = None
+    if not args.no_train and world == 1 and not args.bwd:
+        merge = merge_gbs(st, wl, world)
+        torch.cuda.empty_cache()
+
     e2e = None
     if not args.no_e2e:
         pin = [x.pin_memory() for x in (q_h, k_h, v_h)]
@@ -383,7 +438,7 @@ def run_ours(args, rank, world):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
-            "secondary": train,
+            "secondary": {"train": train, "merge": merge, "mufu": mufu},
         }
         print(json.dumps(line), flush=True)
 

@@ -2,9 +2,10 @@
 // backward row sums Delta, the dQ accumulator conversion and the
 // buffer <-> natural row permutation.
 //
-// All four stream rows of d contiguous elements: one warp per row, lanes
-// moving consecutive 8/16-byte pieces, grid-stride loops over rows with the
-// grid sized to a multiple of the SM count.
+// All four stream rows of d contiguous elements (the merge with 4 elements
+// per thread, the others one warp per row with lanes moving consecutive
+// 8/16-byte pieces), in grid-stride loops over rows with the grid sized to a
+// multiple of the SM count.
 #include <cmath>
 
 #include <cuda_fp16.h>
@@ -31,51 +32,73 @@ int grid_for(int64_t rows) {
 
 // Log-sum-exp merge (ring-attention combine): L = log sum_j exp(lse_j),
 // out = sum_j exp(lse_j - L) O_j; every lse_j = -inf gives L = -inf, out = 0.
+// Each thread owns 4 consecutive elements of a row (16 threads per row at
+// d = 64, 32 at d = 128) and issues the loads of kBatch partials before it
+// combines them, so that enough bytes are in flight to keep HBM busy (one
+// dependent load per partial and warp left the kernel latency-bound).
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32)
 merge_kernel(int nparts, int B, int H, int S, const float* __restrict__ part_out,
              const float* __restrict__ part_lse, T* __restrict__ out, float* __restrict__ lse) {
-    constexpr int PER = D / 32;   // elements per lane (2 or 4)
+    constexpr int TPR = D / 4;     // threads per row
+    constexpr int RPW = 32 / TPR;  // rows per warp
+    constexpr int kBatch = 8;      // partials whose loads are in flight together
     const int lane = threadIdx.x & 31;
+    const int c4 = lane % TPR;
     const int64_t nrows = (int64_t)B * S * H;
     const int64_t elems = nrows * D;
     const int64_t lse_n = (int64_t)B * H * S;
-    for (int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); row < nrows;
-         row += (int64_t)gridDim.x * kWarps) {
+    const int64_t stride = (int64_t)gridDim.x * kWarps * RPW;
+    for (int64_t row = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * RPW + lane / TPR; row < nrows;
+         row += stride) {
         const int h = (int)(row % H);
         const int64_t bs = row / H;
         const int s = (int)(bs % S);
         const int b = (int)(bs / S);
         const int64_t li = ((int64_t)b * H + h) * S + s;
         float m = -INFINITY;
-        for (int j = 0; j < nparts; ++j) m = fmaxf(m, part_lse[j * lse_n + li]);
-        float acc[PER];
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+        for (int j = 0; j < nparts; ++j) m = fmaxf(m, __ldg(part_lse + j * lse_n + li));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         float tot = 0.f;
         if (m != -INFINITY) {
-            for (int j = 0; j < nparts; ++j) {
-                const float w = expf(part_lse[j * lse_n + li] - m);
-                tot += w;
-                const float* src = part_out + j * elems + row * D + lane * PER;
-                if constexpr (PER == 4) {
-                    const float4 x = *reinterpret_cast<const float4*>(src);
-                    acc[0] = fmaf(w, x.x, acc[0]);
-                    acc[1] = fmaf(w, x.y, acc[1]);
-                    acc[PER - 2] = fmaf(w, x.z, acc[PER - 2]);
-                    acc[PER - 1] = fmaf(w, x.w, acc[PER - 1]);
-                } else {
-                    const float2 x = *reinterpret_cast<const float2*>(src);
-                    acc[0] = fmaf(w, x.x, acc[0]);
-                    acc[1] = fmaf(w, x.y, acc[1]);
+            for (int j0 = 0; j0 < nparts; j0 += kBatch) {
+                float4 x[kBatch];
+                float l[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int j = j0 + u;
+                    if (j < nparts) {
+                        x[u] = __ldcs(reinterpret_cast<const float4*>(part_out + j * elems + row * D) + c4);
+                        l[u] = __ldg(part_lse + j * lse_n + li);
+                    } else {
+                        x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        l[u] = -INFINITY;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    if (j0 + u < nparts) {
+                        const float w = expf(l[u] - m);
+                        tot += w;
+                        acc.x = fmaf(w, x[u].x, acc.x);
+                        acc.y = fmaf(w, x[u].y, acc.y);
+                        acc.z = fmaf(w, x[u].z, acc.z);
+                        acc.w = fmaf(w, x[u].w, acc.w);
+                    }
                 }
             }
         }
         const float inv = tot > 0.f ? 1.f / tot : 0.f;
-        T* dst = out + row * D + lane * PER;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) dst[e] = from_f32<T>(acc[e] * inv);
-        if (lane == 0) lse[li] = tot > 0.f ? m + logf(tot) : -INFINITY;
+        T* dst = out + row * D + c4 * 4;
+        if constexpr (sizeof(T) == 4) {
+            *reinterpret_cast<float4*>(dst) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2*>(dst) =
+                make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+        }
+        if (c4 == 0) lse[li] = tot > 0.f ? m + logf(tot) : -INFINITY;
     }
 }
 
