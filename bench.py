@@ -43,6 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 # change without a new capture must drop its entry (traffic is then null).
 NCU_TRAFFIC_BYTES = {"fwd_tc@4218d0c": 8 * (50.380544e6 + 1.218048e6)}
 KERNEL_VERSION = "fwd_tc@4218d0c"
+DEFAULT_WORKLOAD = "vit4096_s65536"
 
 
 def parse():
@@ -50,7 +51,7 @@ def parse():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--workload", default="vit4096_s65536", choices=sorted(WORKLOADS))
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--heads", type=int, default=None,
                    help="override H (a smaller capture of the same sequence shape for ncu)")
@@ -432,7 +433,10 @@ def run_ours(args, rank, world):
             "pct_of_peak": 100.0 * value / world / peak_b,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_b,
                          "unit": "TFLOP/s", "frac": achieved / peak_b,
-                         "traffic": NCU_TRAFFIC_BYTES.get(KERNEL_VERSION),
+                         # the recorded capture is of the default forward workload only
+                         "traffic": (NCU_TRAFFIC_BYTES.get(KERNEL_VERSION)
+                                     if args.workload == DEFAULT_WORKLOAD and not args.bwd and not args.heads
+                                     else None),
                          "peak_kind": peak_kind + " burst bf16"},
             "gpu_launches": args.steps * launches_per_step,
             "e2e": e2e,
