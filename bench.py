@@ -42,7 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 # (2-head capture scaled by 8 to 16 heads: the traffic is per head); a kernel
 # change without a new capture must drop its entry (traffic is then null).
 NCU_TRAFFIC_BYTES = {"fwd_tc@4218d0c": 8 * (50.380544e6 + 1.218048e6)}
-KERNEL_VERSION = "fwd_tc@4218d0c"
+KERNEL_VERSION = "fwd_tc@half-P"
 DEFAULT_WORKLOAD = "vit4096_s65536"
 
 

@@ -69,6 +69,10 @@ struct Cfg {
     // the fp16 P values that weight V -- with no per-score add in the softmax.
     // (d = 128 has no TMEM left for the extra 2 x 16 columns.)
     static constexpr bool kSumCol = D == 64;
+    // d = 64: PV_t in two halves of 64 keys, the first issued as soon as the
+    // softmax has written P for them (at d = 128 the extra live registers of
+    // the early rescale cost more than the earlier PV saves)
+    static constexpr bool kHalfP = D == 64;
     static constexpr int kOCols = D + (kSumCol ? 16 : 0);
     static constexpr int kVStageBytes = kTileBytes + (kSumCol ? kChunkBytes : 0);
     // d = 64: Q is kept in tensor memory as the A operand of S = Q K^T, so
@@ -80,8 +84,8 @@ struct Cfg {
     static constexpr int kKOff = kQOff + (kQTmem ? 0 : kNQ * kTileBytes);
     static constexpr int kVOff = kKOff + kStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kStages * kVStageBytes;
-    // q_full, kv_full[S], kv_empty[S], s_full[NQ], p_full[NQ], o_done[NQ], drain
-    static constexpr int kNumBars = 2 + 2 * kStages + 3 * kNQ;
+    // q_full, kv_full[S], kv_empty[S], s_full[NQ], p_full[NQ], o_done[NQ], drain, p_half[NQ]
+    static constexpr int kNumBars = 2 + 2 * kStages + 4 * kNQ;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -170,6 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     auto bar_p = [&](int t) { return bars + 8u * (1 + 2 * C::kStages + kNQ + t); };
     auto bar_o = [&](int t) { return bars + 8u * (1 + 2 * C::kStages + 2 * kNQ + t); };
     const uint32_t bar_drain = bars + 8u * (1 + 2 * C::kStages + 3 * kNQ);
+    // P_t of keys 0-63 written (PV_t runs in two halves of 64 keys)
+    auto bar_pa = [&](int t) { return bar_drain + 8u * (1 + t); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kMiscOff + 4);
 
@@ -201,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         for (int t = 0; t < kNQ; ++t) {
             mbar_init(bar_s(t), 1);
             mbar_init(bar_p(t), 128);
+            mbar_init(bar_pa(t), 128);
             mbar_init(bar_o(t), 1);
         }
         mbar_init(bar_drain, 1);
@@ -304,25 +311,45 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
                 mma_commit(bar_s(t));
             };
-            // Partial (diagonal / ragged) tiles carry the rows with few visible
-            // keys, whose P entries are large: there P = P_hi + P_lo (both
-            // fp16, P_lo in the upper 64 columns of the S region) and a
-            // second MMA adds P_lo V.
-            auto issue_pv = [&](int t, uint64_t vd, int jj, bool split) {
+            // PV_t in two halves of 64 keys (part 0: keys 0-63, issued as soon
+            // as the softmax has written P for them; part 1 once all of P_t is
+            // in), so that fewer MMAs stand between a finished softmax pass and
+            // the next S_t.  Partial (diagonal / ragged) tiles carry the rows
+            // with few visible keys, whose P entries are large: there P = P_hi
+            // + P_lo (both fp16, P_lo in the upper 64 columns of the S region)
+            // and a second MMA adds P_lo V.
+            // (part 0: keys 0-63, part 1: keys 64-127, part -1: all keys)
+            auto issue_pv = [&](int t, uint64_t vd, int jj, bool split, int part) {
                 const uint32_t tS = tmem + C::s_col(t), tO = tmem + C::o_col(t);
+                const int k0 = part == 1 ? kN / 32 : 0, k1 = part == 0 ? kN / 32 : kN / 16;
 #pragma unroll
                 for (int kk = 0; kk < kN / 16; ++kk)
-                    mma_ts(tO, tS + kk * 8, vd + (uint64_t)(kk * 128), idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                    if (kk >= k0 && kk < k1)
+                        mma_ts(tO, tS + kk * 8, vd + (uint64_t)(kk * 128), idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
                 if (split) {
 #pragma unroll
                     for (int kk = 0; kk < kN / 16; ++kk)
-                        mma_ts(tO, tS + kN / 2 + kk * 8, vd + (uint64_t)(kk * 128), idesc_o, 1u);
+                        if (kk >= k0 && kk < k1)
+                            mma_ts(tO, tS + kN / 2 + kk * 8, vd + (uint64_t)(kk * 128), idesc_o, 1u);
                 }
             };
             bool ok = mbar_wait(bar_q, 0, abort_flag);
             tc_fence_after();
             int j = 0;
             bool split_prev[kNQ] = {false, false};
+            // PV_t(j-1) once P_t(j-1) is written (in two halves at d = 64)
+            auto pv_when_ready = [&](int t, uint64_t vd, int jj) {
+                if constexpr (C::kHalfP) {
+                    ok = mbar_wait(bar_pa(t), jj & 1, abort_flag);
+                    if (!ok) return;
+                    tc_fence_after();
+                    issue_pv(t, vd, jj, split_prev[t], 0);
+                }
+                ok = mbar_wait(bar_p(t), jj & 1, abort_flag);
+                if (!ok) return;
+                tc_fence_after();
+                issue_pv(t, vd, jj, split_prev[t], C::kHalfP ? 1 : -1);
+            };
             // One KV tile.  A tcgen05.commit costs the issuing thread about as
             // much as an MMA, so there are three per tile: S_0, S_1 (each also
             // covers the previous PV of its half, which the softmax relies on
@@ -340,10 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     const int sp = (j - 1) % C::kStages;
                     const uint64_t vd = vdesc + (uint64_t)(sp * (C::kVStageBytes >> 4));
                     for (int t = 0; t < kNQ && ok; ++t) {
-                        ok = mbar_wait(bar_p(t), (j - 1) & 1, abort_flag);
+                        pv_when_ready(t, vd, j - 1);
                         if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(t, vd, j - 1, split_prev[t]);
                         issue_s(t, kd);
                     }
                     if (!ok) return;
@@ -368,10 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const int sp = (j - 1) % C::kStages;
                 const uint64_t vd = vdesc + (uint64_t)(sp * (C::kVStageBytes >> 4));
                 for (int t = 0; t < kNQ && ok; ++t) {
-                    ok = mbar_wait(bar_p(t), (j - 1) & 1, abort_flag);
+                    pv_when_ready(t, vd, j - 1);
                     if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(t, vd, j - 1, split_prev[t]);
                     mma_commit(bar_o(t));   // the epilogue's single wait on O_t
                 }
                 if (ok) mma_commit(bar_e(sp));
@@ -412,6 +435,29 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         float m = -INFINITY, l = 0.f;
         int j = 0;
         bool ok = true;
+        // O_t (and its row-sum column) times alpha when the running max has
+        // grown.  O_t already holds every previous PV product: PV_t(j-1) was
+        // issued before S_t(j), and the commit that signalled S_t(j) covers all
+        // earlier MMAs of the issuing thread.
+        auto rescale_o = [&](float alpha) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tO + c * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                tmem_st32(tO + c * 32, r);
+            }
+            if constexpr (C::kSumCol) {
+                uint32_t r[16];
+                tmem_ld16(tO + D, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                tmem_st16(tO + D, r);
+            }
+        };
         auto step = [&](int nk, int natk) {
             if (!ok || !active(nk, natk)) return;
             ok = __all_sync(0xffffffffu, mbar_wait(bar_s(t), j & 1, abort_flag));
@@ -426,6 +472,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tmem_st16(tS + c * 16, z);
+                if constexpr (C::kHalfP) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar_pa(t));
+                }
             } else {
                 uint32_t sr[4][32];
 #pragma unroll
@@ -469,6 +520,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     constexpr bool kLo = decltype(split_tag)::value;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
+                        if (C::kHalfP && c == 2) {
+                            // keys 0-63 are written: O_t is rescaled first (PV_t(j)
+                            // must not have added to it yet), then PV_t may start on them
+                            if (__any_sync(0xffffffffu, resc) && j > 0) rescale_o(alpha);
+                            tmem_wait_st();
+                            tc_fence_before();
+                            mbar_arrive(bar_pa(t));
+                        }
                         uint32_t pk[16], pl[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
@@ -520,29 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
                 m = m_use;
             }
-            if (__any_sync(0xffffffffu, resc) && j > 0) {
-                // O_t already holds every previous PV product: PV_t(j-1) was
-                // issued before S_t(j), and the commit that signalled S_t(j)
-                // covers all earlier MMAs of the issuing thread
-                {
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(tO + c * 32, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tO + c * 32, r);
-                    }
-                    if constexpr (C::kSumCol) {   // the row-sum column scales with O
-                        uint32_t r[16];
-                        tmem_ld16(tO + D, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st16(tO + D, r);
-                    }
-                }
+            if constexpr (!C::kHalfP) {
+                if (__any_sync(0xffffffffu, resc) && j > 0) rescale_o(alpha);
             }
             tmem_wait_st();
             tc_fence_before();
