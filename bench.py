@@ -230,6 +230,39 @@ def merge_gbs(st, wl, world, steps=10, warmup=3):
             "achieved_gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm, "peak_kind": kind + " HBM copy"}
 
 
+def proj_tflops(st, wl, world, steps=10, warmup=3):
+    """The projections on either side of the attention for the workload's
+    shape (st_proj_gemm, bf16 in, fp32 accumulation, bf16 out): the packed
+    QKV input projection [B*S, H*d] x [3*H*d, H*d]^T and the output
+    projection [B*S, H*d] x [H*d, H*d]^T, random weights."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(13)
+    hidden = wl.H * wl.d
+    M = wl.B * wl.S
+    x = torch.randn((M, hidden), device=dev, generator=g).to(torch.bfloat16)
+    res = {}
+    for name, n_out in (("qkv", 3 * hidden), ("out", hidden)):
+        w = (torch.randn((n_out, hidden), device=dev, generator=g) / hidden ** 0.5).to(torch.bfloat16)
+        y = torch.empty((M, n_out), device=dev, dtype=torch.bfloat16)
+        stream = torch.cuda.current_stream()
+        for _ in range(warmup):
+            st.st_proj_gemm(x, w, out=y, stream=stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            st.st_proj_gemm(x, w, out=y, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+        peak_b, _, _, kind = peaks()
+        tf = 2.0 * M * n_out * hidden / (ms * 1e-3) / 1e12
+        res[name] = {"M": M, "N": n_out, "K": hidden, "ms": ms, "tflops": tf, "frac": tf / peak_b,
+                     "peak_kind": kind + " burst bf16"}
+    return res
+
+
 def train_step_tflops(st, world, steps=3, warmup=2):
     """Forward + backward on the training workload (B=2, H=32, d=128, S=32768,
     causal zigzag over Dirichlet sharding shapes): one step = st_attn_fwd (fp32
@@ -373,9 +406,11 @@ def run_ours(args, rank, world):
         exps = n_exp / (statistics.mean(launch_ms) * 1e-3)
         mufu = {"exps_per_s": exps, "peak_exps_per_s": peak_exp, "frac": exps / peak_exp,
                 "peak_kind": "measured ex2 throughput x 152 SMs x SM clock"}
-    merge = None
+    merge = proj = None
     if not args.no_train and world == 1 and not args.bwd:
         merge = merge_gbs(st, wl, world)
+        torch.cuda.empty_cache()
+        proj = proj_tflops(st, wl, world)
         torch.cuda.empty_cache()
 
     e2e = None
@@ -442,7 +477,7 @@ def run_ours(args, rank, world):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
-            "secondary": {"train": train, "merge": merge, "mufu": mufu},
+            "secondary": {"train": train, "merge": merge, "mufu": mufu, "proj": proj},
         }
         print(json.dumps(line), flush=True)
 

@@ -14,6 +14,7 @@ from ._lib import (  # noqa: F401
     st_attn_merge,
     st_attn_workspace_size,
     st_permute,
+    st_proj_gemm,
     ST_DTYPE_BF16,
     ST_DTYPE_F32,
 )

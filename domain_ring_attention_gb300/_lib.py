@@ -44,6 +44,7 @@ PROTOTYPES = [
     ("st_attn_bwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P, _P, _I, _P, _P, _P,
                          _P, _SZ, _P]),
     ("st_permute", _I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    ("st_proj_gemm", _I, [_I, _I, _I, _P, _P, _P, _I, _P]),
     ("st_error_string", ctypes.c_char_p, [_I]),
     ("st_last_cuda_error", _I, []),
     ("st_device_error", _I, [_P]),
@@ -258,4 +259,24 @@ def st_permute(layout, x, to_natural=True, stream=None):
     out = torch.empty_like(x)
     _check(load().st_permute(layout.handle, B, H, d, _dtype_code(x.dtype), int(bool(to_natural)),
                              _ptr(x), _ptr(out), _stream(stream)), "st_permute")
+    return out
+
+
+def st_proj_gemm(x, w, out_dtype=torch.bfloat16, out=None, stream=None):
+    """Projection y = x w^T on the tensor cores: x [M, K] bf16, w [N, K] bf16
+    (a Linear layer's [out, in] weight) -> y [M, N] in ``out_dtype``.  Leading
+    dimensions of x are flattened (x [..., K] gives y [..., N])."""
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise StAttnError(-3, "st_proj_gemm (bf16 inputs)")
+    if not x.is_contiguous() or not w.is_contiguous():
+        raise StAttnError(-8, "st_proj_gemm (contiguous inputs)")
+    K = int(x.shape[-1])
+    M = x.numel() // max(K, 1)
+    N = int(w.shape[0])
+    if w.dim() != 2 or int(w.shape[1]) != K:
+        raise StAttnError(-8, "st_proj_gemm (weight shape)")
+    if out is None:
+        out = torch.empty(tuple(x.shape[:-1]) + (N,), device=x.device, dtype=out_dtype)
+    _check(load().st_proj_gemm(M, N, K, _ptr(x), _ptr(w), _ptr(out), _dtype_code(out.dtype), _stream(stream)),
+           "st_proj_gemm")
     return out

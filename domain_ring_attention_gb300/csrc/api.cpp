@@ -55,8 +55,18 @@ extern "C" int st_device_error(void* stream) {
     if (rc != ST_OK) return rc;
     const int f = st::fwd_tc_device_error(true);
     const int b = st::bwd_tc_device_error(true);
-    if (f < 0 || b < 0) return cuda_status((int)cudaGetLastError());
-    return (f || b) ? ST_ERR_DEVICE_TIMEOUT : ST_OK;
+    const int g = st::gemm_tc_device_error(true);
+    if (f < 0 || b < 0 || g < 0) return cuda_status((int)cudaGetLastError());
+    return (f || b || g) ? ST_ERR_DEVICE_TIMEOUT : ST_OK;
+}
+
+extern "C" int st_proj_gemm(int M, int N, int K, const void* x, const void* w, void* y, int out_dtype,
+                            void* stream) {
+    if (!x || !w || !y) return ST_ERR_NULL;
+    if (M < 1 || N < 1 || K < 1 || N % 8 != 0 || K % 8 != 0) return ST_ERR_INVALID_ARG;
+    if (out_dtype != ST_DTYPE_BF16 && out_dtype != ST_DTYPE_F32) return ST_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return ST_ERR_MISALIGNED;
+    return cuda_status(st::launch_gemm_tc(M, N, K, x, w, y, out_dtype, stream));
 }
 
 namespace st {

@@ -107,6 +107,9 @@ int launch_bwd_tc(const st_layout& L, const BwdArgs& a, void* stream, bool* hand
 // up, -1 if it could not be read); clear resets it.
 int fwd_tc_device_error(bool clear);
 int bwd_tc_device_error(bool clear);
+int gemm_tc_device_error(bool clear);
+// C[M, N] = A[M, K] W[N, K]^T on the tensor cores (bf16 in, fp32 accumulation)
+int launch_gemm_tc(int M, int N, int K, const void* a, const void* w, void* c, int out_dtype, void* stream);
 int launch_merge(int D, int B, int H, int64_t S, int d, const float* part_out,
                  const float* part_lse, void* out, float* lse, int out_dtype, void* stream);
 int launch_bwd_preprocess(const BwdArgs& a, int64_t S, int dtype, void* stream);

@@ -195,6 +195,33 @@ int st_attn_bwd(const st_layout_t* layout, int B, int H, int d, int dtype, int c
 int st_permute(const st_layout_t* layout, int B, int H, int d, int dtype, int to_natural,
                const void* in, void* out, void* stream);
 
+/*
+ * Projection GEMM:  y[M, N] = x[M, K] w[N, K]^T.
+ *
+ * The projections on either side of the attention (TSP summary, "Folding
+ * Tensor and Sequence Parallelism", section 2, attention layer, broadcast
+ * schedule: every rank computes the local projections of its sequence shard
+ * with each packed W_Q, W_K, W_V, W_O weight shard in turn).  On one GPU the
+ * sequence shards are row ranges of x (in buffer order) and the weight shards
+ * row ranges of w, so every (sequence shard, weight shard) product is a block
+ * of this one product: for the input projections x is [B*S, hidden] and w the
+ * packed [3*H*d, hidden] W_Q|W_K|W_V, whose output viewed as [B, S, 3, H, d]
+ * holds q, k and v; for the output projection x is the attention output
+ * [B*S, H*d] and w is W_O [hidden, H*d].
+ *
+ *   x   : device, bf16, [M, K] row-major.
+ *   w   : device, bf16, [N, K] row-major (a Linear layer's [out, in] weight).
+ *   y   : device, [M, N] row-major, out_dtype ST_DTYPE_BF16 or ST_DTYPE_F32.
+ *   Tensor cores with fp32 accumulation over K.  N and K must be multiples of
+ *   8 (16-byte rows for the TMA), pointers 16-byte aligned.
+ *
+ * Returns ST_ERR_NULL, ST_ERR_INVALID_ARG (sizes), ST_ERR_UNSUPPORTED (dtype),
+ * ST_ERR_MISALIGNED or ST_ERR_CUDA.  The caller owns every buffer; nothing is
+ * allocated.
+ */
+int st_proj_gemm(int M, int N, int K, const void* x, const void* w, void* y, int out_dtype,
+                 void* stream);
+
 /* Wait for `stream`, then report (and clear) the device error word of the
  * tensor-core kernels: ST_ERR_DEVICE_TIMEOUT if one of their bounded
  * barrier waits gave up since the last call (the kernel then stopped early

@@ -17,6 +17,11 @@ What it computes, and where each part comes from:
                        summary, section 2, all-gathered K/V + FlashAttention,
                        which computes the same function as full attention.)
   * ``bruteforce``  -- pure-Python loops for tiny inputs.
+  * ``projection``  -- the linear layers on either side of the attention, by
+                       their definition and by the broadcast schedule of the
+                       pages (TSP summary, section 2, attention layer: every
+                       rank projects its sequence shard with each packed
+                       W_Q, W_K, W_V, W_O shard in turn).
 
 All floating point is float64 on the values the caller passes (for bf16 inputs
 the caller passes the bf16-rounded values).  Every function is pinned by tests
@@ -24,4 +29,4 @@ that do not re-type its formula: a library attention routine, closed forms,
 invariants the pages fix (sharded == unsharded, zigzag-causal == causal) and
 finite differences.
 """
-from . import layout, attention, bruteforce  # noqa: F401
+from . import layout, attention, bruteforce, projection  # noqa: F401

@@ -111,6 +111,14 @@ def test_bad_calls_return_codes_without_a_gpu(lib):
     assert mrg(2, 1, 1, 64, 96, good, good, good, lse, 0, None) == -3
     assert lib.st_permute(lay.handle, 1, 1, 64, 1, 1, good, good, None) == -8
     assert lib.st_error_string(-4).decode().startswith("a tensor pointer")
+    gemm = lib.st_proj_gemm
+    assert gemm(64, 256, 64, None, good, good, 1, None) == -1
+    assert gemm(64, 256, 64, good, good, None, 1, None) == -1
+    assert gemm(0, 256, 64, good, good, good, 1, None) == -8
+    assert gemm(64, 252, 64, good, good, good, 1, None) == -8      # N not a multiple of 8
+    assert gemm(64, 256, 60, good, good, good, 1, None) == -8      # K not a multiple of 8
+    assert gemm(64, 256, 64, good, good, good, 2, None) == -3
+    assert gemm(64, 256, 64, P(0x10004), good, good, 1, None) == -4
 
 
 def test_python_binding_refuses_cpu_tensors(lib):
