@@ -22,6 +22,10 @@ What it computes, and where each part comes from:
                        pages (TSP summary, section 2, attention layer: every
                        rank projects its sequence shard with each packed
                        W_Q, W_K, W_V, W_O shard in turn).
+  * ``mlp``         -- the gated MLP by its definition and by the pages'
+                       ring schedule (TSP summary, section 2, gated MLP
+                       layer: W1, W2, W3 shards travel round the ring while
+                       every rank adds up its partial outputs).
 
 All floating point is float64 on the values the caller passes (for bf16 inputs
 the caller passes the bf16-rounded values).  Every function is pinned by tests
@@ -29,4 +33,4 @@ that do not re-type its formula: a library attention routine, closed forms,
 invariants the pages fix (sharded == unsharded, zigzag-causal == causal) and
 finite differences.
 """
-from . import layout, attention, bruteforce, projection  # noqa: F401
+from . import layout, attention, bruteforce, projection, mlp  # noqa: F401
