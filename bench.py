@@ -263,6 +263,38 @@ def proj_tflops(st, wl, world, steps=10, warmup=3):
     return res
 
 
+def mlp_tflops(st, world, steps=10, warmup=3):
+    """The gated MLP that TSP pairs with its ring schedule (st_gated_mlp: the
+    gate and up GEMM with the SiLU-gated epilogue, then the down GEMM), at the
+    7B-style width (hidden 4096 = 32 heads x 128, F = 11008) over 65536 tokens,
+    random weights; 6*M*hidden*F flops per call."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(17)
+    M, hidden, F = 65536, 4096, 11008
+    x = torch.randn((M, hidden), device=dev, generator=g).to(torch.bfloat16)
+    w1 = (torch.randn((F, hidden), device=dev, generator=g) / hidden ** 0.5).to(torch.bfloat16)
+    w3 = (torch.randn((F, hidden), device=dev, generator=g) / hidden ** 0.5).to(torch.bfloat16)
+    w2 = (torch.randn((hidden, F), device=dev, generator=g) / F ** 0.5).to(torch.bfloat16)
+    h = torch.empty((M, F), device=dev, dtype=torch.bfloat16)
+    y = torch.empty((M, hidden), device=dev, dtype=torch.bfloat16)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        st.st_gated_mlp(x, w1, w3, w2, out=y, h=h, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        st.st_gated_mlp(x, w1, w3, w2, out=y, h=h, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    peak_b, _, _, kind = peaks()
+    tf = 6.0 * M * hidden * F / (ms * 1e-3) / 1e12
+    return {"M": M, "hidden": hidden, "F": F, "ms": ms, "tflops": tf, "frac": tf / peak_b,
+            "peak_kind": kind + " burst bf16", "launches": 2}
+
+
 def train_step_tflops(st, world, steps=3, warmup=2):
     """Forward + backward on the training workload (B=2, H=32, d=128, S=32768,
     causal zigzag over Dirichlet sharding shapes): one step = st_attn_fwd (fp32
@@ -406,11 +438,13 @@ def run_ours(args, rank, world):
         exps = n_exp / (statistics.mean(launch_ms) * 1e-3)
         mufu = {"exps_per_s": exps, "peak_exps_per_s": peak_exp, "frac": exps / peak_exp,
                 "peak_kind": "measured ex2 throughput x 152 SMs x SM clock"}
-    merge = proj = None
+    merge = proj = mlp = None
     if not args.no_train and world == 1 and not args.bwd:
         merge = merge_gbs(st, wl, world)
         torch.cuda.empty_cache()
         proj = proj_tflops(st, wl, world)
+        torch.cuda.empty_cache()
+        mlp = mlp_tflops(st, world)
         torch.cuda.empty_cache()
 
     e2e = None
@@ -477,7 +511,7 @@ def run_ours(args, rank, world):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
-            "secondary": {"train": train, "merge": merge, "mufu": mufu, "proj": proj},
+            "secondary": {"train": train, "merge": merge, "mufu": mufu, "proj": proj, "mlp": mlp},
         }
         print(json.dumps(line), flush=True)
 

@@ -15,6 +15,7 @@ from ._lib import (  # noqa: F401
     st_attn_workspace_size,
     st_permute,
     st_proj_gemm,
+    st_gated_mlp,
     ST_DTYPE_BF16,
     ST_DTYPE_F32,
 )

@@ -45,6 +45,7 @@ PROTOTYPES = [
                          _P, _SZ, _P]),
     ("st_permute", _I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     ("st_proj_gemm", _I, [_I, _I, _I, _P, _P, _P, _I, _P]),
+    ("st_gated_mlp", _I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
     ("st_error_string", ctypes.c_char_p, [_I]),
     ("st_last_cuda_error", _I, []),
     ("st_device_error", _I, [_P]),
@@ -280,3 +281,30 @@ def st_proj_gemm(x, w, out_dtype=torch.bfloat16, out=None, stream=None):
     _check(load().st_proj_gemm(M, N, K, _ptr(x), _ptr(w), _ptr(out), _dtype_code(out.dtype), _stream(stream)),
            "st_proj_gemm")
     return out
+
+
+def st_gated_mlp(x, w1, w3, w2, out_dtype=torch.bfloat16, out=None, h=None, stream=None):
+    """Gated MLP y = (silu(x w1^T) * (x w3^T)) w2^T on the tensor cores:
+    x [..., hidden] bf16, w1 and w3 [F, hidden] bf16, w2 [hidden, F] bf16 ->
+    y [..., hidden] in ``out_dtype``.  ``h`` ([M, F] bf16) receives the gated
+    activation; it is allocated when not given.  Returns (y, h)."""
+    ws = (x, w1, w3, w2)
+    if any(t.dtype != torch.bfloat16 for t in ws):
+        raise StAttnError(-3, "st_gated_mlp (bf16 inputs)")
+    if not all(t.is_contiguous() for t in ws):
+        raise StAttnError(-8, "st_gated_mlp (contiguous inputs)")
+    hidden = int(x.shape[-1])
+    M = x.numel() // max(hidden, 1)
+    F = int(w1.shape[0])
+    if (w1.dim() != 2 or tuple(w1.shape) != (F, hidden) or tuple(w3.shape) != (F, hidden)
+            or tuple(w2.shape) != (hidden, F)):
+        raise StAttnError(-8, "st_gated_mlp (weight shapes)")
+    if h is None:
+        h = torch.empty((M, F), device=x.device, dtype=torch.bfloat16)
+    elif h.dtype != torch.bfloat16 or h.numel() != M * F or not h.is_contiguous():
+        raise StAttnError(-8, "st_gated_mlp (h workspace)")
+    if out is None:
+        out = torch.empty(tuple(x.shape[:-1]) + (hidden,), device=x.device, dtype=out_dtype)
+    _check(load().st_gated_mlp(M, hidden, F, _ptr(x), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(h), _ptr(out),
+                               _dtype_code(out.dtype), _stream(stream)), "st_gated_mlp")
+    return out, h

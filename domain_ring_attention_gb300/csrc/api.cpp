@@ -69,6 +69,18 @@ extern "C" int st_proj_gemm(int M, int N, int K, const void* x, const void* w, v
     return cuda_status(st::launch_gemm_tc(M, N, K, x, w, y, out_dtype, stream));
 }
 
+extern "C" int st_gated_mlp(int M, int hidden, int F, const void* x, const void* w1, const void* w3,
+                            const void* w2, void* h, void* y, int out_dtype, void* stream) {
+    if (!x || !w1 || !w3 || !w2 || !h || !y) return ST_ERR_NULL;
+    if (M < 1 || hidden < 1 || F < 1 || hidden % 8 != 0 || F % 8 != 0) return ST_ERR_INVALID_ARG;
+    if (out_dtype != ST_DTYPE_BF16 && out_dtype != ST_DTYPE_F32) return ST_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) || !aligned16(h) || !aligned16(y))
+        return ST_ERR_MISALIGNED;
+    int rc = cuda_status(st::launch_gemm_gated(M, F, hidden, x, w1, w3, h, stream));
+    if (rc != ST_OK) return rc;
+    return cuda_status(st::launch_gemm_tc(M, hidden, F, h, w2, y, out_dtype, stream));
+}
+
 namespace st {
 
 BwdWorkspace bwd_workspace_layout(int64_t rows, int d, int dtype) {

@@ -110,6 +110,8 @@ int bwd_tc_device_error(bool clear);
 int gemm_tc_device_error(bool clear);
 // C[M, N] = A[M, K] W[N, K]^T on the tensor cores (bf16 in, fp32 accumulation)
 int launch_gemm_tc(int M, int N, int K, const void* a, const void* w, void* c, int out_dtype, void* stream);
+// h[M, F] = silu(a w1^T) * (a w3^T), bf16 (gemm_tc.cu)
+int launch_gemm_gated(int M, int F, int K, const void* a, const void* w1, const void* w3, void* h, void* stream);
 int launch_merge(int D, int B, int H, int64_t S, int d, const float* part_out,
                  const float* part_lse, void* out, float* lse, int out_dtype, void* stream);
 int launch_bwd_preprocess(const BwdArgs& a, int64_t S, int dtype, void* stream);

@@ -22,6 +22,12 @@
 //              bf16 / fp32 -> global memory (rows and columns past M, N are
 //              not stored; K past the end is zero-filled by the TMA).
 // Every barrier wait is bounded (tc_ptx.cuh).
+//
+// Gated variant (the gate and up projections of a gated MLP, TSP summary,
+// section 2, gated MLP layer): the 256 rows of the W tile are 128 rows of W1
+// followed by the same 128 rows of W3, so one MMA tile holds the gate
+// a = x W1^T and the up value b = x W3^T for 128 hidden units side by side,
+// and the epilogue writes h = silu(a) * b (bf16) for those 128 columns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -53,8 +59,9 @@ static_assert(kGSmemBytes <= 232448, "shared memory per CTA");
 
 struct GemmParams {
     CUtensorMap ta;     // A: (K, M) bf16, box (64, 128), 128-byte swizzle
-    CUtensorMap tw;     // W: (K, N) bf16, box (64, 256), 128-byte swizzle
-    void* c;            // [M, N] bf16 or fp32
+    CUtensorMap tw;     // W: (K, N) bf16, box (64, 256); gated: W1, box (64, 128)
+    CUtensorMap tw3;    // gated only: W3 (K, N) bf16, box (64, 128)
+    void* c;            // [M, N] bf16 or fp32 (gated: h, bf16)
     int M, N, K;
     int out_f32;
 };
@@ -72,7 +79,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// x * sigmoid(x), with the exponential from the CUDA intrinsic; exp(-x) = inf
+// for very negative x gives -0, the limit.
+__device__ __forceinline__ float silu(float x) { return x / (1.f + __expf(-x)); }
+
+template <bool kGated>
 __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+    constexpr int kTN = kGated ? kGN / 2 : kGN;   // output columns per tile
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -88,7 +101,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kGMiscOff + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_m = (p.M + kGM - 1) / kGM, tiles_n = (p.N + kGN - 1) / kGN;
+    const int tiles_m = (p.M + kGM - 1) / kGM, tiles_n = (p.N + kTN - 1) / kTN;
     const int ntiles = tiles_m * tiles_n;
     const int nkb = (p.K + kGK - 1) / kGK;
 
@@ -112,6 +125,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&p.ta);
         prefetch_tmap(&p.tw);
+        if (kGated) prefetch_tmap(&p.tw3);
     }
     tc_fence_before();
     __syncthreads();
@@ -124,14 +138,16 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
             int it = 0;   // K blocks issued so far (over all tiles)
             bool ok = true;
             for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                const int m0 = (tile / tiles_n) * kGM, n0 = (tile % tiles_n) * kGN;
+                const int m0 = (tile / tiles_n) * kGM, n0 = (tile % tiles_n) * kTN;
                 for (int kb = 0; kb < nkb && ok; ++kb, ++it) {
                     const int s = it % kGStages;
                     if (it >= kGStages) ok = mbar_wait(bar_empty(s), ((it / kGStages) - 1) & 1, abort_flag);
                     if (!ok) break;
+                    // both gated boxes are full 128-row boxes (rows past N zero-filled)
                     mbar_arrive_expect_tx(bar_full(s), kABytes + kWBytes);
                     tma_load_2d(sA + s * kABytes, &p.ta, bar_full(s), kb * kGK, m0);
                     tma_load_2d(sW + s * kWBytes, &p.tw, bar_full(s), kb * kGK, n0);
+                    if (kGated) tma_load_2d(sW + s * kWBytes + kWBytes / 2, &p.tw3, bar_full(s), kb * kGK, n0);
                 }
             }
             // every load issued lands before the CTA can exit (also after an abort)
@@ -182,7 +198,34 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
             ok = __all_sync(0xffffffffu, mbar_wait(bar_accf(a), (nt >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const int row = (tile / tiles_n) * kGM + r, n0 = (tile % tiles_n) * kGN;
+            const int row = (tile / tiles_n) * kGM + r, n0 = (tile % tiles_n) * kTN;
+            if constexpr (kGated) {
+#pragma unroll 1
+                for (int c = 0; c < kTN / 32; ++c) {
+                    uint32_t ga[32], up[32];
+                    tmem_ld32(lane_base + (uint32_t)(a * kGN + c * 32), ga);
+                    tmem_ld32(lane_base + (uint32_t)(a * kGN + kTN + c * 32), up);
+                    tmem_wait_ld();
+                    const int col = n0 + c * 32;
+                    if (row < p.M && col < p.N) {
+                        const int ngrp = min(4, (p.N - col) / 8);
+                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.c) + (int64_t)row * p.N + col;
+                        float h[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) h[i] = silu(__uint_as_float(ga[i])) * __uint_as_float(up[i]);
+#pragma unroll
+                        for (int g = 0; g < 4; ++g)
+                            if (g < ngrp)
+                                *reinterpret_cast<uint4*>(dst + 8 * g) =
+                                    make_uint4(pack_bf16x2(h[8 * g], h[8 * g + 1]), pack_bf16x2(h[8 * g + 2], h[8 * g + 3]),
+                                               pack_bf16x2(h[8 * g + 4], h[8 * g + 5]),
+                                               pack_bf16x2(h[8 * g + 6], h[8 * g + 7]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(bar_acce(a));
+                continue;
+            }
 #pragma unroll 1
             for (int c = 0; c < kGN / 32; ++c) {
                 uint32_t v[32];
@@ -267,16 +310,8 @@ bool make_map_2d(CUtensorMap* m, const void* base, int rows, int K, int box_rows
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-int launch_gemm_tc(int M, int N, int K, const void* a, const void* w, void* c, int out_dtype, void* stream) {
-    GemmParams p;
-    if (!make_map_2d(&p.ta, a, M, K, kGM) || !make_map_2d(&p.tw, w, N, K, kGN)) return (int)cudaErrorInvalidValue;
-    p.c = c;
-    p.M = M;
-    p.N = N;
-    p.K = K;
-    p.out_f32 = out_dtype == ST_DTYPE_F32 ? 1 : 0;
+template <bool kGated>
+int launch(const GemmParams& p, void* stream) {
     static int sms = 0;
     if (sms == 0) {
         int dev = 0;
@@ -284,12 +319,41 @@ int launch_gemm_tc(int M, int N, int K, const void* a, const void* w, void* c, i
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms <= 0) sms = 1;
     }
-    const int ntiles = ((M + kGM - 1) / kGM) * ((N + kGN - 1) / kGN);
+    const int tn = kGated ? kGN / 2 : kGN;
+    const int ntiles = ((p.M + kGM - 1) / kGM) * ((p.N + tn - 1) / tn);
     const int grid = ntiles < sms ? ntiles : sms;
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemBytes);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_kernel<kGated>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemBytes);
     if (e != cudaSuccess) return (int)e;
-    gemm_tc_kernel<<<grid, kGThreads, kGSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
+    gemm_tc_kernel<kGated><<<grid, kGThreads, kGSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
     return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_gemm_tc(int M, int N, int K, const void* a, const void* w, void* c, int out_dtype, void* stream) {
+    GemmParams p;
+    if (!make_map_2d(&p.ta, a, M, K, kGM) || !make_map_2d(&p.tw, w, N, K, kGN)) return (int)cudaErrorInvalidValue;
+    p.tw3 = p.tw;
+    p.c = c;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.out_f32 = out_dtype == ST_DTYPE_F32 ? 1 : 0;
+    return launch<false>(p, stream);
+}
+
+int launch_gemm_gated(int M, int F, int K, const void* a, const void* w1, const void* w3, void* h, void* stream) {
+    GemmParams p;
+    if (!make_map_2d(&p.ta, a, M, K, kGM) || !make_map_2d(&p.tw, w1, F, K, kGN / 2) ||
+        !make_map_2d(&p.tw3, w3, F, K, kGN / 2))
+        return (int)cudaErrorInvalidValue;
+    p.c = h;
+    p.M = M;
+    p.N = F;
+    p.K = K;
+    p.out_f32 = 0;
+    return launch<true>(p, stream);
 }
 
 int gemm_tc_device_error(bool clear) {

@@ -222,6 +222,36 @@ int st_permute(const st_layout_t* layout, int B, int H, int d, int dtype, int to
 int st_proj_gemm(int M, int N, int K, const void* x, const void* w, void* y, int out_dtype,
                  void* stream);
 
+/*
+ * Gated MLP:  h = silu(x W1^T) * (x W3^T),  y = h W2^T,  silu(a) = a / (1 + e^-a).
+ *
+ * The feed-forward layer that TSP pairs with its ring schedule (TSP summary,
+ * "Folding Tensor and Sequence Parallelism", section 2, gated MLP layer: the
+ * W1, W2, W3 shards travel round the ring while each rank keeps its tokens
+ * and adds up its partial outputs, so no all-reduce is needed).  A weight
+ * shard j is a range F_j of hidden units: rows F_j of W1 and W3 and columns
+ * F_j of W2.  The partial output of shard j is silu(x W1_j^T) * (x W3_j^T)
+ * W2_j^T, and the partials over all shards sum to the product above.  On one
+ * GPU every shard is resident, so the sum over shards is the K loop of the
+ * second GEMM, over all F hidden units.
+ *
+ *   x   : device, bf16, [M, hidden] row-major (M tokens in buffer order).
+ *   w1  : device, bf16, [F, hidden] (gate weight, a Linear layer's [out, in]).
+ *   w3  : device, bf16, [F, hidden] (up weight).
+ *   w2  : device, bf16, [hidden, F] (down weight).
+ *   h   : device, bf16, [M, F]: caller-owned workspace; holds the gated
+ *         activation on return (rounded once to bf16 from fp32 accumulators,
+ *         then the A operand of the down projection).
+ *   y   : device, [M, hidden], out_dtype ST_DTYPE_BF16 or ST_DTYPE_F32.
+ *   hidden and F must be multiples of 8, pointers 16-byte aligned.  Two
+ *   tensor-core launches on `stream`; fp32 accumulation in both.
+ *
+ * Returns ST_ERR_NULL, ST_ERR_INVALID_ARG (sizes), ST_ERR_UNSUPPORTED (dtype),
+ * ST_ERR_MISALIGNED or ST_ERR_CUDA.  Nothing is allocated.
+ */
+int st_gated_mlp(int M, int hidden, int F, const void* x, const void* w1, const void* w3, const void* w2,
+                 void* h, void* y, int out_dtype, void* stream);
+
 /* Wait for `stream`, then report (and clear) the device error word of the
  * tensor-core kernels: ST_ERR_DEVICE_TIMEOUT if one of their bounded
  * barrier waits gave up since the last call (the kernel then stopped early

@@ -119,6 +119,15 @@ def test_bad_calls_return_codes_without_a_gpu(lib):
     assert gemm(64, 256, 60, good, good, good, 1, None) == -8      # K not a multiple of 8
     assert gemm(64, 256, 64, good, good, good, 2, None) == -3
     assert gemm(64, 256, 64, P(0x10004), good, good, 1, None) == -4
+    mlp = lib.st_gated_mlp
+    w = [good] * 3
+    assert mlp(64, 256, 512, None, *w, good, good, 1, None) == -1
+    assert mlp(64, 256, 512, good, *w, None, good, 1, None) == -1          # h workspace
+    assert mlp(0, 256, 512, good, *w, good, good, 1, None) == -8
+    assert mlp(64, 252, 512, good, *w, good, good, 1, None) == -8          # hidden not a multiple of 8
+    assert mlp(64, 256, 500, good, *w, good, good, 1, None) == -8          # F not a multiple of 8
+    assert mlp(64, 256, 512, good, *w, good, good, 2, None) == -3
+    assert mlp(64, 256, 512, good, good, P(0x10004), good, good, good, 1, None) == -4
 
 
 def test_python_binding_refuses_cpu_tensors(lib):
