@@ -26,6 +26,12 @@ What it computes, and where each part comes from:
                        ring schedule (TSP summary, section 2, gated MLP
                        layer: W1, W2, W3 shards travel round the ring while
                        every rank adds up its partial outputs).
+  * ``halo``        -- 2-D convolution of a row-sharded image with uneven
+                       shards: the halo exchange (neighbouring rows taken
+                       from the shards that own them) and the local
+                       convolutions, equal to the layer on the whole image
+                       (ShardTensor summary, section 2, communication: halo
+                       exchange for convolution and normalisation).
 
 All floating point is float64 on the values the caller passes (for bf16 inputs
 the caller passes the bf16-rounded values).  Every function is pinned by tests
@@ -33,4 +39,4 @@ that do not re-type its formula: a library attention routine, closed forms,
 invariants the pages fix (sharded == unsharded, zigzag-causal == causal) and
 finite differences.
 """
-from . import layout, attention, bruteforce, projection, mlp  # noqa: F401
+from . import layout, attention, bruteforce, projection, mlp, halo  # noqa: F401
