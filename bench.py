@@ -295,6 +295,44 @@ def mlp_tflops(st, world, steps=10, warmup=3):
             "peak_kind": kind + " burst bf16", "launches": 2}
 
 
+def conv_tflops(st, world, steps=10, warmup=3):
+    """Halo exchange + 2-D convolution of a row-sharded image (st_halo_exchange
+    then st_conv2d_sharded): the CONUS grid 1024 x 1792, 256 channels in and
+    out, 3 x 3 kernel, D = 4 Dirichlet-uneven row shards, bf16 in and out,
+    random weights.  2*H*W*C_in*C_out*k*k flops per step; the inputs (0.94 GB)
+    and outputs exceed L2."""
+    from domain_ring_attention_gb300.workloads import dirichlet_shard_lengths
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(19)
+    H, W, C, k = 1024, 1792, 256, 3
+    rows = dirichlet_shard_lengths(H, 4, seed=0, multiple=1)
+    shards = [torch.randn((L + 2, W, C), device=dev, generator=g).to(torch.bfloat16) for L in rows]
+    w = (torch.randn((C, k, k, C), device=dev, generator=g) / (k * k * C) ** 0.5).to(torch.bfloat16)
+    b = torch.zeros((C,), device=dev)
+    out = [torch.empty((L, W, C), device=dev, dtype=torch.bfloat16) for L in rows]
+    stream = torch.cuda.current_stream()
+
+    def step():
+        st.st_halo_exchange(shards, 1, stream=stream)
+        st.st_conv2d_sharded(shards, w, b, out=out, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    peak_b, _, _, kind = peaks()
+    tf = 2.0 * H * W * C * C * k * k / (ms * 1e-3) / 1e12
+    return {"H": H, "W": W, "C_in": C, "C_out": C, "k": k, "shard_rows": rows, "ms": ms, "tflops": tf,
+            "frac": tf / peak_b, "peak_kind": kind + " burst bf16", "launches": 2}
+
+
 def train_step_tflops(st, world, steps=3, warmup=2):
     """Forward + backward on the training workload (B=2, H=32, d=128, S=32768,
     causal zigzag over Dirichlet sharding shapes): one step = st_attn_fwd (fp32
@@ -438,13 +476,15 @@ def run_ours(args, rank, world):
         exps = n_exp / (statistics.mean(launch_ms) * 1e-3)
         mufu = {"exps_per_s": exps, "peak_exps_per_s": peak_exp, "frac": exps / peak_exp,
                 "peak_kind": "measured ex2 throughput x 152 SMs x SM clock"}
-    merge = proj = mlp = None
+    merge = proj = mlp = conv = None
     if not args.no_train and world == 1 and not args.bwd:
         merge = merge_gbs(st, wl, world)
         torch.cuda.empty_cache()
         proj = proj_tflops(st, wl, world)
         torch.cuda.empty_cache()
         mlp = mlp_tflops(st, world)
+        torch.cuda.empty_cache()
+        conv = conv_tflops(st, world)
         torch.cuda.empty_cache()
 
     e2e = None
@@ -511,7 +551,7 @@ def run_ours(args, rank, world):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
-            "secondary": {"train": train, "merge": merge, "mufu": mufu, "proj": proj, "mlp": mlp},
+            "secondary": {"train": train, "merge": merge, "mufu": mufu, "proj": proj, "mlp": mlp, "conv": conv},
         }
         print(json.dumps(line), flush=True)
 

@@ -16,6 +16,8 @@ from ._lib import (  # noqa: F401
     st_permute,
     st_proj_gemm,
     st_gated_mlp,
+    st_halo_exchange,
+    st_conv2d_sharded,
     ST_DTYPE_BF16,
     ST_DTYPE_F32,
 )

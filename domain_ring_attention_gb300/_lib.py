@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libst_attn.so")
 ST_DTYPE_F32 = 0
 ST_DTYPE_BF16 = 1
 ST_MAX_SHARDS = 32
+ST_CONV_MAX_SHARDS = 16
 
 ERRORS = {
     0: "ST_OK", -1: "ST_ERR_NULL", -2: "ST_ERR_INVALID_LAYOUT", -3: "ST_ERR_UNSUPPORTED",
@@ -46,6 +47,9 @@ PROTOTYPES = [
     ("st_permute", _I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     ("st_proj_gemm", _I, [_I, _I, _I, _P, _P, _P, _I, _P]),
     ("st_gated_mlp", _I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
+    ("st_halo_exchange", _I, [_I, ctypes.POINTER(_I64), _I, _I, _I, ctypes.POINTER(_P), _P]),
+    ("st_conv2d_sharded", _I, [_I, ctypes.POINTER(_I64), _I, _I, _I, _I, ctypes.POINTER(_P), _P, _P,
+                               ctypes.POINTER(_P), _I, _P]),
     ("st_error_string", ctypes.c_char_p, [_I]),
     ("st_last_cuda_error", _I, []),
     ("st_device_error", _I, [_P]),
@@ -308,3 +312,61 @@ def st_gated_mlp(x, w1, w3, w2, out_dtype=torch.bfloat16, out=None, h=None, stre
     _check(load().st_gated_mlp(M, hidden, F, _ptr(x), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(h), _ptr(out),
                                _dtype_code(out.dtype), _stream(stream)), "st_gated_mlp")
     return out, h
+
+
+def _ptr_array(ts):
+    return (_P * len(ts))(*[t.data_ptr() for t in ts])
+
+
+def _image_shards(shards, pad, name):
+    """Shard lengths and the common (W, C) of a list of channels-last shards
+    [L_r + 2*pad, W, C]."""
+    if not shards:
+        raise StAttnError(-8, name + " (no shards)")
+    W, C = int(shards[0].shape[1]), int(shards[0].shape[2])
+    rows = []
+    for t in shards:
+        if t.dim() != 3 or int(t.shape[1]) != W or int(t.shape[2]) != C or not t.is_contiguous():
+            raise StAttnError(-8, name + " (shards must be contiguous [rows, W, C] with one W and C)")
+        rows.append(int(t.shape[0]) - 2 * pad)
+    return rows, W, C
+
+
+def st_halo_exchange(shards, halo, stream=None):
+    """Fill, in place, the ``halo`` pad rows above and below every shard of a
+    row-sharded image.  ``shards``: list of D bf16 tensors [L_r + 2*halo, W, C]
+    (channels last) whose middle L_r rows hold the shard's image rows, in
+    order.  Pad rows receive the neighbouring image rows (zeros outside the
+    image).  Returns ``shards``."""
+    if any(t.dtype != torch.bfloat16 for t in shards):
+        raise StAttnError(-3, "st_halo_exchange (bf16 shards)")
+    rows, W, C = _image_shards(shards, halo, "st_halo_exchange")
+    D = len(shards)
+    _check(load().st_halo_exchange(D, (_I64 * D)(*rows), W, C, int(halo), _ptr_array(shards), _stream(stream)),
+           "st_halo_exchange")
+    return shards
+
+
+def st_conv2d_sharded(shards, weight, bias=None, out_dtype=torch.bfloat16, out=None, stream=None):
+    """2-D convolution (cross-correlation, stride 1, zero padding (k-1)/2) of a
+    row-sharded image from halo-padded shards, one output per shard.
+    ``shards``: list of D bf16 tensors [L_r + k - 1, W, C_in] after
+    st_halo_exchange(shards, (k-1)//2); ``weight``: bf16 [C_out, k, k, C_in];
+    ``bias``: fp32 [C_out] or None.  Returns the list of [L_r, W, C_out]."""
+    if weight.dtype != torch.bfloat16 or any(t.dtype != torch.bfloat16 for t in shards):
+        raise StAttnError(-3, "st_conv2d_sharded (bf16 inputs)")
+    if weight.dim() != 4 or weight.shape[1] != weight.shape[2] or not weight.is_contiguous():
+        raise StAttnError(-8, "st_conv2d_sharded (weight [C_out, k, k, C_in])")
+    C_out, k, C_in = int(weight.shape[0]), int(weight.shape[1]), int(weight.shape[3])
+    rows, W, C = _image_shards(shards, (k - 1) // 2, "st_conv2d_sharded")
+    if C != C_in:
+        raise StAttnError(-8, "st_conv2d_sharded (channels of shards and weight differ)")
+    if bias is not None and (bias.dtype != torch.float32 or bias.numel() != C_out or not bias.is_contiguous()):
+        raise StAttnError(-8, "st_conv2d_sharded (bias fp32 [C_out])")
+    if out is None:
+        out = [torch.empty((max(L, 0), W, C_out), device=shards[0].device, dtype=out_dtype) for L in rows]
+    D = len(shards)
+    _check(load().st_conv2d_sharded(D, (_I64 * D)(*rows), W, C_in, C_out, k, _ptr_array(shards), _ptr(weight),
+                                    _ptr(bias), _ptr_array(out), _dtype_code(out[0].dtype), _stream(stream)),
+           "st_conv2d_sharded")
+    return out

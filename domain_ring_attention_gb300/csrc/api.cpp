@@ -56,8 +56,9 @@ extern "C" int st_device_error(void* stream) {
     const int f = st::fwd_tc_device_error(true);
     const int b = st::bwd_tc_device_error(true);
     const int g = st::gemm_tc_device_error(true);
-    if (f < 0 || b < 0 || g < 0) return cuda_status((int)cudaGetLastError());
-    return (f || b || g) ? ST_ERR_DEVICE_TIMEOUT : ST_OK;
+    const int c = st::conv_tc_device_error(true);
+    if (f < 0 || b < 0 || g < 0 || c < 0) return cuda_status((int)cudaGetLastError());
+    return (f || b || g || c) ? ST_ERR_DEVICE_TIMEOUT : ST_OK;
 }
 
 extern "C" int st_proj_gemm(int M, int N, int K, const void* x, const void* w, void* y, int out_dtype,
@@ -67,6 +68,51 @@ extern "C" int st_proj_gemm(int M, int N, int K, const void* x, const void* w, v
     if (out_dtype != ST_DTYPE_BF16 && out_dtype != ST_DTYPE_F32) return ST_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return ST_ERR_MISALIGNED;
     return cuda_status(st::launch_gemm_tc(M, N, K, x, w, y, out_dtype, stream));
+}
+
+namespace {
+
+// shared checks of the sharded-image entry points; rows are host values
+int check_image_shards(int D, const int64_t* rows, int W, void* const* shards) {
+    if (!rows || !shards) return ST_ERR_NULL;
+    if (D < 1 || D > ST_CONV_MAX_SHARDS || W < 1) return ST_ERR_INVALID_ARG;
+    int64_t H = 0;
+    for (int r = 0; r < D; ++r) {
+        if (rows[r] < 1) return ST_ERR_INVALID_LAYOUT;
+        H += rows[r];
+        if (!shards[r]) return ST_ERR_NULL;
+        if (!aligned16(shards[r])) return ST_ERR_MISALIGNED;
+    }
+    if (H > (1 << 24)) return ST_ERR_INVALID_ARG;
+    return ST_OK;
+}
+
+}  // namespace
+
+extern "C" int st_halo_exchange(int D, const int64_t* rows, int W, int C, int halo, void* const* shards,
+                                void* stream) {
+    int rc = check_image_shards(D, rows, W, shards);
+    if (rc != ST_OK) return rc;
+    if (C < 8 || C % 8 != 0 || halo < 0 || halo > 3) return ST_ERR_INVALID_ARG;
+    if ((int64_t)W * C > (1 << 24)) return ST_ERR_INVALID_ARG;
+    return cuda_status(st::launch_halo_exchange(D, rows, W, C, halo, shards, stream));
+}
+
+extern "C" int st_conv2d_sharded(int D, const int64_t* rows, int W, int C_in, int C_out, int k,
+                                 void* const* in_shards, const void* weight, const float* bias,
+                                 void* const* out_shards, int out_dtype, void* stream) {
+    int rc = check_image_shards(D, rows, W, in_shards);
+    if (rc != ST_OK) return rc;
+    rc = check_image_shards(D, rows, W, out_shards);
+    if (rc != ST_OK) return rc;
+    if (!weight) return ST_ERR_NULL;
+    if (k < 1 || k > 7 || k % 2 == 0 || C_in < 64 || C_in % 64 != 0 || C_in > 4096 || C_out < 8 ||
+        C_out % 8 != 0 || C_out > 4096)
+        return ST_ERR_INVALID_ARG;
+    if (out_dtype != ST_DTYPE_BF16 && out_dtype != ST_DTYPE_F32) return ST_ERR_UNSUPPORTED;
+    if (!aligned16(weight) || (bias && reinterpret_cast<uintptr_t>(bias) % 4 != 0)) return ST_ERR_MISALIGNED;
+    return cuda_status(
+        st::launch_conv_tc(D, rows, W, C_in, C_out, k, in_shards, weight, bias, out_shards, out_dtype, stream));
 }
 
 extern "C" int st_gated_mlp(int M, int hidden, int F, const void* x, const void* w1, const void* w3,

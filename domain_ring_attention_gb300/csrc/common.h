@@ -108,8 +108,13 @@ int launch_bwd_tc(const st_layout& L, const BwdArgs& a, void* stream, bool* hand
 int fwd_tc_device_error(bool clear);
 int bwd_tc_device_error(bool clear);
 int gemm_tc_device_error(bool clear);
+int conv_tc_device_error(bool clear);
 // C[M, N] = A[M, K] W[N, K]^T on the tensor cores (bf16 in, fp32 accumulation)
 int launch_gemm_tc(int M, int N, int K, const void* a, const void* w, void* c, int out_dtype, void* stream);
+// halo exchange and sharded 2-D convolution (conv_tc.cu)
+int launch_halo_exchange(int D, const int64_t* rows, int W, int C, int h, void* const* shards, void* stream);
+int launch_conv_tc(int D, const int64_t* rows, int W, int C_in, int C_out, int k, void* const* in_shards,
+                   const void* weight, const float* bias, void* const* out_shards, int out_dtype, void* stream);
 // h[M, F] = silu(a w1^T) * (a w3^T), bf16 (gemm_tc.cu)
 int launch_gemm_gated(int M, int F, int K, const void* a, const void* w1, const void* w3, void* h, void* stream);
 int launch_merge(int D, int B, int H, int64_t S, int d, const float* part_out,

@@ -63,6 +63,7 @@ enum {
 enum { ST_DTYPE_F32 = 0, ST_DTYPE_BF16 = 1 };
 
 enum { ST_MAX_SHARDS = 32 };
+enum { ST_CONV_MAX_SHARDS = 16 };   /* shards of st_halo_exchange / st_conv2d_sharded */
 
 /* Opaque, host-resident shard-layout descriptor.  Thread-safe to read from
  * several host threads at once; create and destroy are not synchronised. */
@@ -251,6 +252,66 @@ int st_proj_gemm(int M, int N, int K, const void* x, const void* w, void* y, int
  */
 int st_gated_mlp(int M, int hidden, int F, const void* x, const void* w1, const void* w3, const void* w2,
                  void* h, void* y, int out_dtype, void* stream);
+
+/*
+ * Halo exchange of a row-sharded image.
+ *
+ * ShardTensor summary, "ShardTensor" section 2, implementation details,
+ * communication: a convolution or normalisation over a spatially sharded
+ * input needs the neighbouring pixels held by the adjacent chunks (the
+ * "halo").  The H image rows are split into D shards of rows[r] >= 1 rows
+ * (uneven sharding shapes, section 2), in order.  Shard r is its own buffer,
+ * as it would be on its own device.
+ *
+ *   rows   : host, D values; the image has H = sum(rows) rows.
+ *   shards : host array of D device pointers.  shards[r] is bf16
+ *            [rows[r] + 2*halo, W, C] (channels last).  Its rows
+ *            halo .. halo + rows[r] - 1 hold image rows off_r .. off_r + rows[r] - 1,
+ *            where off_r = rows[0] + ... + rows[r-1].
+ *   Fills, in place, the halo rows above and below each shard's own rows with
+ *   the image rows off_r - halo .. off_r - 1 and off_r + rows[r] ..
+ *   off_r + rows[r] + halo - 1, taken from whichever shards own them (a shard
+ *   shorter than halo passes on rows of shards further away).  Rows outside
+ *   the image are written as zeros.  Only pad rows are written, only own rows
+ *   read.
+ *   1 <= D <= ST_CONV_MAX_SHARDS, 0 <= halo <= 3, C a multiple of 8,
+ *   W*C <= 2^24, H <= 2^24; pointers 16-byte aligned.  One launch on `stream`.
+ *
+ * Returns ST_ERR_NULL, ST_ERR_INVALID_LAYOUT (a shard of < 1 row),
+ * ST_ERR_INVALID_ARG, ST_ERR_MISALIGNED or ST_ERR_CUDA.  Nothing is allocated.
+ */
+int st_halo_exchange(int D, const int64_t* rows, int W, int C, int halo, void* const* shards, void* stream);
+
+/*
+ * 2-D convolution of a row-sharded image, from halo-padded shards.
+ *
+ *   y_r[i, j, o] = bias[o] + sum_{u,v,c} xpad_r[i + u, j + v - h, c] * w[o, u, v, c]
+ *
+ * Here h = (k - 1) / 2. xpad_r is shard r padded with h rows on each side, as
+ * st_halo_exchange leaves it, and it is zero outside 0 <= j + v - h < W.
+ * After the exchange, the shards' outputs stacked in order are the
+ * cross-correlation of the whole image: the convolution of deep-learning
+ * layers, stride 1, zero padding h, output as large as the input. That is the
+ * reading this library takes of the convolution the same passage names.
+ *
+ *   rows       : host, D shard lengths (as st_halo_exchange).
+ *   in_shards  : host array of D device pointers, bf16 [rows[r] + 2h, W, C_in].
+ *   weight     : device, bf16 [C_out, k, k, C_in] (channels last).
+ *   bias       : device fp32 [C_out], or NULL for none.
+ *   out_shards : host array of D device pointers, [rows[r], W, C_out] in
+ *                out_dtype (ST_DTYPE_BF16 or ST_DTYPE_F32).
+ *   Tensor cores: bf16 products, fp32 accumulation over k*k*C_in.
+ *   k odd in 1..7; C_in a multiple of 64 (<= 4096); C_out a multiple of 8
+ *   (<= 4096); 1 <= D <= ST_CONV_MAX_SHARDS; pointers 16-byte aligned.  One
+ *   launch on `stream`.
+ *
+ * Returns ST_ERR_NULL, ST_ERR_INVALID_LAYOUT, ST_ERR_INVALID_ARG,
+ * ST_ERR_UNSUPPORTED (dtype), ST_ERR_MISALIGNED or ST_ERR_CUDA.  Nothing is
+ * allocated.
+ */
+int st_conv2d_sharded(int D, const int64_t* rows, int W, int C_in, int C_out, int k, void* const* in_shards,
+                      const void* weight, const float* bias, void* const* out_shards, int out_dtype,
+                      void* stream);
 
 /* Wait for `stream`, then report (and clear) the device error word of the
  * tensor-core kernels: ST_ERR_DEVICE_TIMEOUT if one of their bounded

@@ -128,6 +128,29 @@ def test_bad_calls_return_codes_without_a_gpu(lib):
     assert mlp(64, 256, 500, good, *w, good, good, 1, None) == -8          # F not a multiple of 8
     assert mlp(64, 256, 512, good, *w, good, good, 2, None) == -3
     assert mlp(64, 256, 512, good, good, P(0x10004), good, good, good, 1, None) == -4
+    rows = (ctypes.c_int64 * 3)(5, 1, 7)
+    shards = (P * 3)(0x10000, 0x20000, 0x30000)
+    halo = lib.st_halo_exchange
+    assert halo(3, None, 16, 64, 1, shards, None) == -1
+    assert halo(3, rows, 16, 64, 1, None, None) == -1
+    assert halo(0, rows, 16, 64, 1, shards, None) == -8
+    assert halo(17, rows, 16, 64, 1, shards, None) == -8            # more shards than ST_CONV_MAX_SHARDS
+    assert halo(3, rows, 16, 60, 1, shards, None) == -8             # C not a multiple of 8
+    assert halo(3, rows, 16, 64, 4, shards, None) == -8             # halo > 3
+    assert halo(3, (ctypes.c_int64 * 3)(5, 0, 7), 16, 64, 1, shards, None) == -2
+    assert halo(3, rows, 16, 64, 1, (P * 3)(0x10000, None, 0x30000), None) == -1
+    assert halo(3, rows, 16, 64, 1, (P * 3)(0x10000, 0x20008, 0x30000), None) == -4
+    conv = lib.st_conv2d_sharded
+    outs = (P * 3)(0x40000, 0x50000, 0x60000)
+    assert conv(3, rows, 16, 64, 128, 3, shards, None, None, outs, 1, None) == -1
+    assert conv(3, rows, 16, 64, 128, 3, shards, good, None, None, 1, None) == -1
+    assert conv(3, rows, 16, 64, 128, 4, shards, good, None, outs, 1, None) == -8   # even kernel
+    assert conv(3, rows, 16, 64, 128, 9, shards, good, None, outs, 1, None) == -8   # k > 7
+    assert conv(3, rows, 16, 96, 128, 3, shards, good, None, outs, 1, None) == -8   # C_in not a multiple of 64
+    assert conv(3, rows, 16, 64, 100, 3, shards, good, None, outs, 1, None) == -8   # C_out not a multiple of 8
+    assert conv(3, rows, 16, 64, 128, 3, shards, good, None, outs, 2, None) == -3
+    assert conv(3, rows, 16, 64, 128, 3, shards, P(0x10004), None, outs, 1, None) == -4
+    assert conv(3, rows, 16, 64, 128, 3, shards, good, P(0x10002), outs, 1, None) == -4
 
 
 def test_python_binding_refuses_cpu_tensors(lib):
