@@ -198,6 +198,14 @@ MUFU_EX2_PER_CLK_SM = 30.5
 GB300_SMS = 152
 
 
+def cool_down(seconds=1.0):
+    """Free cached blocks and let the GPU idle before the next secondary
+    measurement (outside every timed region)."""
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    time.sleep(seconds)
+
+
 def merge_gbs(st, wl, world, steps=10, warmup=3):
     """Standalone log-sum-exp merge (st_attn_merge) of D per-KV-shard partials
     of the workload's shape: HBM-bound, reported as algorithmic GB/s (partials
@@ -478,14 +486,16 @@ def run_ours(args, rank, world):
                 "peak_kind": "measured ex2 throughput x 152 SMs x SM clock"}
     merge = proj = mlp = conv = None
     if not args.no_train and world == 1 and not args.bwd:
+        # each after a pause, so that none starts under the power cap that the
+        # previous one ran into; the gated MLP, which draws the most, goes last
         merge = merge_gbs(st, wl, world)
-        torch.cuda.empty_cache()
+        cool_down()
         proj = proj_tflops(st, wl, world)
-        torch.cuda.empty_cache()
-        mlp = mlp_tflops(st, world)
-        torch.cuda.empty_cache()
+        cool_down()
         conv = conv_tflops(st, world)
-        torch.cuda.empty_cache()
+        cool_down()
+        mlp = mlp_tflops(st, world)
+        cool_down()
 
     e2e = None
     if not args.no_e2e:
@@ -521,6 +531,8 @@ def run_ours(args, rank, world):
         e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
+    if not args.no_train:
+        cool_down()
     train = None if args.no_train else train_step_tflops(st, world)
 
     cpu = None

@@ -9,9 +9,10 @@
 // all (sequence shard x weight shard) products is this one GEMM over all rows
 // in buffer order.
 //
-// Persistent kernel: one CTA per SM walks the 128 x 256 output tiles
-// (row-block major, so the CTAs working at one time share rows of A in L2
-// and W stays L2-resident).  Warp roles (192 threads):
+// Persistent kernel: one CTA per SM walks the 128 x 256 output tiles in
+// groups of row blocks (tile_coords), so the CTAs working at one time share
+// a few row blocks of A and a few column blocks of W in L2 even when W is
+// larger than L2.  Warp roles (192 threads):
 //   warp 0     TMA producer: 64-wide K blocks of A (128 rows) and W (256 rows)
 //              into a 4-stage shared-memory ring;
 //   warp 1     TMEM allocator and single-thread MMA issuer: 4 MMAs
@@ -57,6 +58,18 @@ constexpr int kGMiscOff = kGBarOff + kGNumBars * 8;
 constexpr int kGSmemBytes = kGMiscOff + 16 + 1024;
 static_assert(kGSmemBytes <= 232448, "shared memory per CTA");
 
+// Output tile t -> (row block, column block).  Tiles are taken in groups of
+// `group` row blocks; inside a group the column block is the slow index.  The
+// CTAs working at one time then share a few row blocks of A and a few column
+// blocks of W, both small enough to stay in L2, instead of all of W.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group, int& mb, int& nb) {
+    const int per_group = group * tiles_n;
+    const int g = t / per_group, local = t % per_group;
+    const int gm = min(group, tiles_m - g * group);
+    mb = g * group + local % gm;
+    nb = local / gm;
+}
+
 struct GemmParams {
     CUtensorMap ta;     // A: (K, M) bf16, box (64, 128), 128-byte swizzle
     CUtensorMap tw;     // W: (K, N) bf16, box (64, 256); gated: W1, box (64, 128)
@@ -64,6 +77,7 @@ struct GemmParams {
     void* c;            // [M, N] bf16 or fp32 (gated: h, bf16)
     int M, N, K;
     int out_f32;
+    int group;          // row blocks per tile group (tile_coords)
 };
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint32_t bar, int c0, int c1) {
@@ -138,7 +152,9 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
             int it = 0;   // K blocks issued so far (over all tiles)
             bool ok = true;
             for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                const int m0 = (tile / tiles_n) * kGM, n0 = (tile % tiles_n) * kTN;
+                int mb, nb;
+                tile_coords(tile, tiles_m, tiles_n, p.group, mb, nb);
+                const int m0 = mb * kGM, n0 = nb * kTN;
                 for (int kb = 0; kb < nkb && ok; ++kb, ++it) {
                     const int s = it % kGStages;
                     if (it >= kGStages) ok = mbar_wait(bar_empty(s), ((it / kGStages) - 1) & 1, abort_flag);
@@ -198,7 +214,9 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
             ok = __all_sync(0xffffffffu, mbar_wait(bar_accf(a), (nt >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const int row = (tile / tiles_n) * kGM + r, n0 = (tile % tiles_n) * kTN;
+            int mb, nb;
+            tile_coords(tile, tiles_m, tiles_n, p.group, mb, nb);
+            const int row = mb * kGM + r, n0 = nb * kTN;
             if constexpr (kGated) {
 #pragma unroll 1
                 for (int c = 0; c < kTN / 32; ++c) {
@@ -311,7 +329,7 @@ bool make_map_2d(CUtensorMap* m, const void* base, int rows, int K, int box_rows
 }
 
 template <bool kGated>
-int launch(const GemmParams& p, void* stream) {
+int launch(GemmParams p, void* stream) {
     static int sms = 0;
     if (sms == 0) {
         int dev = 0;
@@ -320,7 +338,16 @@ int launch(const GemmParams& p, void* stream) {
         if (sms <= 0) sms = 1;
     }
     const int tn = kGated ? kGN / 2 : kGN;
-    const int ntiles = ((p.M + kGM - 1) / kGM) * ((p.N + tn - 1) / tn);
+    const int tiles_m = (p.M + kGM - 1) / kGM;
+    const int ntiles = tiles_m * ((p.N + tn - 1) / tn);
+    // A W of at most 32 MB stays in L2 whole: take the tiles row block by row
+    // block (group 1), so that the CTAs working at one time share A rows.  A
+    // larger W is taken in groups of row blocks whose A rows (kGM x K bf16
+    // each) fit in 32 MB, column block by column block within the group.
+    const int64_t w_bytes = (int64_t)p.N * p.K * 2;
+    const int64_t a_block = (int64_t)kGM * p.K * 2;
+    int64_t group = w_bytes <= ((int64_t)32 << 20) ? 1 : ((int64_t)32 << 20) / a_block;
+    p.group = (int)(group < 1 ? 1 : (group > tiles_m ? tiles_m : group));
     const int grid = ntiles < sms ? ntiles : sms;
     cudaError_t e =
         cudaFuncSetAttribute(gemm_tc_kernel<kGated>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemBytes);
