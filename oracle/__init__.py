@@ -32,6 +32,9 @@ What it computes, and where each part comes from:
                        convolutions, equal to the layer on the whole image
                        (ShardTensor summary, section 2, communication: halo
                        exchange for convolution and normalisation).
+  * ``norm``        -- group normalisation of a row-sharded image: local
+                       statistics, their all-reduce, local normalisation
+                       (the same passage: collectives for normalisation).
 
 All floating point is float64 on the values the caller passes (for bf16 inputs
 the caller passes the bf16-rounded values).  Every function is pinned by tests
@@ -39,4 +42,4 @@ that do not re-type its formula: a library attention routine, closed forms,
 invariants the pages fix (sharded == unsharded, zigzag-causal == causal) and
 finite differences.
 """
-from . import layout, attention, bruteforce, projection, mlp, halo  # noqa: F401
+from . import layout, attention, bruteforce, projection, mlp, halo, norm  # noqa: F401
