@@ -341,6 +341,42 @@ def conv_tflops(st, world, steps=10, warmup=3):
             "frac": tf / peak_b, "peak_kind": kind + " burst bf16", "launches": 2}
 
 
+def norm_gbs(st, world, steps=10, warmup=3):
+    """Group normalisation of the row-sharded CONUS grid (st_group_norm_sharded:
+    statistics, their all-reduce over the shards, normalisation): 1024 x 1792
+    pixels, 256 channels in 32 groups, four Dirichlet-uneven row shards, bf16
+    in and out.  HBM-bound, reported as algorithmic GB/s: the statistics need
+    every value before the first output, so x is read twice and y written
+    once (3 x 0.94 GB); x exceeds L2."""
+    from domain_ring_attention_gb300.workloads import dirichlet_shard_lengths
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(23)
+    H, W, C, G = 1024, 1792, 256, 32
+    rows = dirichlet_shard_lengths(H, 4, seed=0, multiple=1)
+    xs = [torch.randn((L, W, C), device=dev, generator=g).to(torch.bfloat16) for L in rows]
+    out = [torch.empty((L, W, C), device=dev, dtype=torch.bfloat16) for L in rows]
+    gamma = torch.ones(C, device=dev)
+    beta = torch.zeros(C, device=dev)
+    ws = torch.empty(1 << 20, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        st.st_group_norm_sharded(xs, G, gamma, beta, out=out, workspace=ws, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        st.st_group_norm_sharded(xs, G, gamma, beta, out=out, workspace=ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    nbytes = 3 * H * W * C * 2
+    _, _, hbm, kind = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"H": H, "W": W, "C": C, "G": G, "shard_rows": rows, "bytes_per_step": nbytes, "ms": ms,
+            "achieved_gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm, "peak_kind": kind + " HBM copy", "launches": 3}
+
+
 def train_step_tflops(st, world, steps=3, warmup=2):
     """Forward + backward on the training workload (B=2, H=32, d=128, S=32768,
     causal zigzag over Dirichlet sharding shapes): one step = st_attn_fwd (fp32
@@ -484,7 +520,7 @@ def run_ours(args, rank, world):
         exps = n_exp / (statistics.mean(launch_ms) * 1e-3)
         mufu = {"exps_per_s": exps, "peak_exps_per_s": peak_exp, "frac": exps / peak_exp,
                 "peak_kind": "measured ex2 throughput x 152 SMs x SM clock"}
-    merge = proj = mlp = conv = None
+    merge = proj = mlp = conv = gnorm = None
     if not args.no_train and world == 1 and not args.bwd:
         # each after a pause, so that none starts under the power cap that the
         # previous one ran into; the gated MLP, which draws the most, goes last
@@ -493,6 +529,8 @@ def run_ours(args, rank, world):
         proj = proj_tflops(st, wl, world)
         cool_down()
         conv = conv_tflops(st, world)
+        cool_down()
+        gnorm = norm_gbs(st, world)
         cool_down()
         mlp = mlp_tflops(st, world)
         cool_down()
@@ -563,7 +601,7 @@ def run_ours(args, rank, world):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
-            "secondary": {"train": train, "merge": merge, "mufu": mufu, "proj": proj, "mlp": mlp, "conv": conv},
+            "secondary": {"train": train, "merge": merge, "mufu": mufu, "proj": proj, "mlp": mlp, "conv": conv, "norm": gnorm},
         }
         print(json.dumps(line), flush=True)
 

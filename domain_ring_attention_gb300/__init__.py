@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     st_gated_mlp,
     st_halo_exchange,
     st_conv2d_sharded,
+    st_group_norm_sharded,
     ST_DTYPE_BF16,
     ST_DTYPE_F32,
 )

@@ -50,6 +50,9 @@ PROTOTYPES = [
     ("st_halo_exchange", _I, [_I, ctypes.POINTER(_I64), _I, _I, _I, ctypes.POINTER(_P), _P]),
     ("st_conv2d_sharded", _I, [_I, ctypes.POINTER(_I64), _I, _I, _I, _I, ctypes.POINTER(_P), _P, _P,
                                ctypes.POINTER(_P), _I, _P]),
+    ("st_group_norm_workspace_size", _I, [_I, _I, ctypes.POINTER(_SZ)]),
+    ("st_group_norm_sharded", _I, [_I, ctypes.POINTER(_I64), _I, _I, _I, _F, ctypes.POINTER(_P), _P, _P,
+                                   ctypes.POINTER(_P), _I, _I, _P, _SZ, _P]),
     ("st_error_string", ctypes.c_char_p, [_I]),
     ("st_last_cuda_error", _I, []),
     ("st_device_error", _I, [_P]),
@@ -369,4 +372,31 @@ def st_conv2d_sharded(shards, weight, bias=None, out_dtype=torch.bfloat16, out=N
     _check(load().st_conv2d_sharded(D, (_I64 * D)(*rows), W, C_in, C_out, k, _ptr_array(shards), _ptr(weight),
                                     _ptr(bias), _ptr_array(out), _dtype_code(out[0].dtype), _stream(stream)),
            "st_conv2d_sharded")
+    return out
+
+
+def st_group_norm_sharded(shards, G, gamma=None, beta=None, eps=1e-5, out_dtype=torch.bfloat16, out=None,
+                          out_pad=0, workspace=None, stream=None):
+    """Group normalisation of a row-sharded image with statistics combined
+    over all shards.  ``shards``: list of D bf16 tensors [L_r, W, C];
+    ``gamma``/``beta``: fp32 [C] or None.  Returns the list of outputs
+    [L_r + 2*out_pad, W, C] (pad rows untouched)."""
+    if any(t.dtype != torch.bfloat16 for t in shards):
+        raise StAttnError(-3, "st_group_norm_sharded (bf16 shards)")
+    rows, W, C = _image_shards(shards, 0, "st_group_norm_sharded")
+    for name, t in (("gamma", gamma), ("beta", beta)):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != C or not t.is_contiguous()):
+            raise StAttnError(-8, "st_group_norm_sharded (%s fp32 [C])" % name)
+    lib = load()
+    n = ctypes.c_size_t()
+    _check(lib.st_group_norm_workspace_size(C, int(G), ctypes.byref(n)), "st_group_norm_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(n.value, device=shards[0].device, dtype=torch.uint8)
+    if out is None:
+        out = [torch.zeros((L + 2 * out_pad, W, C), device=shards[0].device, dtype=out_dtype) for L in rows]
+    D = len(shards)
+    _check(lib.st_group_norm_sharded(D, (_I64 * D)(*rows), W, C, int(G), float(eps), _ptr_array(shards),
+                                     _ptr(gamma), _ptr(beta), _ptr_array(out), int(out_pad),
+                                     _dtype_code(out[0].dtype), _ptr(workspace), workspace.numel(),
+                                     _stream(stream)), "st_group_norm_sharded")
     return out

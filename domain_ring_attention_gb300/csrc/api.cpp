@@ -115,6 +115,46 @@ extern "C" int st_conv2d_sharded(int D, const int64_t* rows, int W, int C_in, in
         st::launch_conv_tc(D, rows, W, C_in, C_out, k, in_shards, weight, bias, out_shards, out_dtype, stream));
 }
 
+namespace {
+
+int check_group_norm(int C, int G) {
+    // C / 8 vectors per pixel must divide the 256 threads of a block
+    if (C < 8 || C > 2048 || (C & (C - 1)) != 0) return ST_ERR_INVALID_ARG;
+    if (G < 1 || C % G != 0 || (C / G) % 8 != 0) return ST_ERR_INVALID_ARG;
+    return ST_OK;
+}
+
+}  // namespace
+
+extern "C" int st_group_norm_workspace_size(int C, int G, size_t* bytes) {
+    if (!bytes) return ST_ERR_NULL;
+    const int rc = check_group_norm(C, G);
+    if (rc != ST_OK) return rc;
+    *bytes = st::group_norm_workspace_bytes(G);
+    return ST_OK;
+}
+
+extern "C" int st_group_norm_sharded(int D, const int64_t* rows, int W, int C, int G, float eps,
+                                     const void* const* in_shards, const float* gamma, const float* beta,
+                                     void* const* out_shards, int out_pad, int out_dtype, void* workspace,
+                                     size_t ws_bytes, void* stream) {
+    int rc = check_image_shards(D, rows, W, const_cast<void* const*>(in_shards));
+    if (rc != ST_OK) return rc;
+    rc = check_image_shards(D, rows, W, out_shards);
+    if (rc != ST_OK) return rc;
+    rc = check_group_norm(C, G);
+    if (rc != ST_OK) return rc;
+    if (!(eps > 0.f) || out_pad < 0 || out_pad > 3) return ST_ERR_INVALID_ARG;
+    if (out_dtype != ST_DTYPE_BF16 && out_dtype != ST_DTYPE_F32) return ST_ERR_UNSUPPORTED;
+    if ((gamma && reinterpret_cast<uintptr_t>(gamma) % 4) || (beta && reinterpret_cast<uintptr_t>(beta) % 4))
+        return ST_ERR_MISALIGNED;
+    if (!workspace) return ST_ERR_WORKSPACE;
+    if (ws_bytes < st::group_norm_workspace_bytes(G)) return ST_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ST_ERR_MISALIGNED;
+    return cuda_status(st::launch_group_norm(D, rows, W, C, G, eps, in_shards, gamma, beta, out_shards, out_pad,
+                                             out_dtype, workspace, stream));
+}
+
 extern "C" int st_gated_mlp(int M, int hidden, int F, const void* x, const void* w1, const void* w3,
                             const void* w2, void* h, void* y, int out_dtype, void* stream) {
     if (!x || !w1 || !w3 || !w2 || !h || !y) return ST_ERR_NULL;

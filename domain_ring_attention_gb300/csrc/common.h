@@ -115,6 +115,12 @@ int launch_gemm_tc(int M, int N, int K, const void* a, const void* w, void* c, i
 int launch_halo_exchange(int D, const int64_t* rows, int W, int C, int h, void* const* shards, void* stream);
 int launch_conv_tc(int D, const int64_t* rows, int W, int C_in, int C_out, int k, void* const* in_shards,
                    const void* weight, const float* bias, void* const* out_shards, int out_dtype, void* stream);
+// group normalisation of a row-sharded image (norm.cu)
+constexpr int kGnStatBlocks = 2048;   // most statistics blocks (sizes the workspace)
+size_t group_norm_workspace_bytes(int G);
+int launch_group_norm(int D, const int64_t* rows, int W, int C, int G, float eps, const void* const* in,
+                      const float* gamma, const float* beta, void* const* out, int out_pad, int out_dtype,
+                      void* workspace, void* stream);
 // h[M, F] = silu(a w1^T) * (a w3^T), bf16 (gemm_tc.cu)
 int launch_gemm_gated(int M, int F, int K, const void* a, const void* w1, const void* w3, void* h, void* stream);
 int launch_merge(int D, int B, int H, int64_t S, int d, const float* part_out,

@@ -313,6 +313,45 @@ int st_conv2d_sharded(int D, const int64_t* rows, int W, int C_in, int C_out, in
                       const void* weight, const float* bias, void* const* out_shards, int out_dtype,
                       void* stream);
 
+/*
+ * Group normalisation of a row-sharded image.
+ *
+ * ShardTensor summary, "ShardTensor" section 2, implementation details,
+ * communication: normalisation over a spatially sharded input needs a
+ * collective, here the all-reduce of per-group statistics, to give the
+ * numbers of the layer on the whole image.  Group normalisation is the
+ * reading this library takes of the normalisation that passage names.
+ *
+ *   y[i, j, c] = (x[i, j, c] - mu_g) / sqrt(var_g + eps) * gamma[c] + beta[c]
+ *
+ * Channel c is in group g = c / (C / G).  mu_g and var_g (biased) are taken
+ * over every pixel of every shard and every channel of the group.
+ *
+ *   rows       : host, D shard lengths (image rows), as st_halo_exchange.
+ *   in_shards  : host array of D device pointers, bf16 [rows[r], W, C].
+ *   gamma, beta: device fp32 [C], or NULL for 1 and 0.
+ *   out_shards : host array of D device pointers, [rows[r] + 2*out_pad, W, C]
+ *                in out_dtype (ST_DTYPE_BF16 or ST_DTYPE_F32).  Rows
+ *                out_pad .. out_pad + rows[r] - 1 are written and the pad rows
+ *                left as they are, so the output can go straight into
+ *                st_halo_exchange and st_conv2d_sharded (out_pad = (k-1)/2).
+ *   workspace  : device, >= st_group_norm_workspace_size bytes, 16-byte
+ *                aligned; the per-block statistics and the combined mean and
+ *                1/std per group (fp64) are left there.
+ *   C a power of two in 8 .. 2048; C a multiple of G; C / G a multiple of 8;
+ *   eps > 0; 0 <= out_pad <= 3; 1 <= D <= ST_CONV_MAX_SHARDS.
+ *   Statistics are kept in fp32 per thread (shifted sums), merged in fp32
+ *   per block and in fp64 across blocks.  Three launches on `stream`.
+ *
+ * Returns ST_ERR_NULL, ST_ERR_INVALID_LAYOUT, ST_ERR_INVALID_ARG,
+ * ST_ERR_UNSUPPORTED (dtype), ST_ERR_MISALIGNED, ST_ERR_WORKSPACE or
+ * ST_ERR_CUDA.  Nothing is allocated.
+ */
+int st_group_norm_workspace_size(int C, int G, size_t* bytes);
+int st_group_norm_sharded(int D, const int64_t* rows, int W, int C, int G, float eps, const void* const* in_shards,
+                          const float* gamma, const float* beta, void* const* out_shards, int out_pad,
+                          int out_dtype, void* workspace, size_t ws_bytes, void* stream);
+
 /* Wait for `stream`, then report (and clear) the device error word of the
  * tensor-core kernels: ST_ERR_DEVICE_TIMEOUT if one of their bounded
  * barrier waits gave up since the last call (the kernel then stopped early

@@ -84,14 +84,17 @@ def sharded_group_norm(x, shard_rows, G, gamma=None, beta=None, eps=1e-5):
     if off[-1] != len(x) or min(shard_rows) < 1:
         raise ValueError("shard lengths must be >= 1 and cover the rows")
     chunks = [x[off[r]:off[r + 1]] for r in range(len(shard_rows))]
-    n, mean, m2 = all_reduce([local_stats(c, G) for c in chunks])
+    stats = all_reduce([local_stats(c, G) for c in chunks])
+    return [normalize(c, stats, G, gamma, beta, eps) for c in chunks]
+
+
+def normalize(chunk, stats, G, gamma=None, beta=None, eps=1e-5):
+    """Rows of one shard normalised with the combined statistics (n, mean, M2)."""
+    n, mean, m2 = stats
     rstd = 1.0 / np.sqrt(m2 / n + eps)
-    C = x.shape[2]
+    chunk = np.asarray(chunk, dtype=np.float64)
+    C = chunk.shape[2]
     g = np.ones(C) if gamma is None else np.asarray(gamma, dtype=np.float64)
     b = np.zeros(C) if beta is None else np.asarray(beta, dtype=np.float64)
-    out = []
-    for c in chunks:
-        cg = _groups(c, G)
-        y = ((cg - mean[None, :, None]) * rstd[None, :, None]).reshape(c.shape)
-        out.append(y * g + b)
-    return out
+    y = ((_groups(chunk, G) - mean[None, :, None]) * rstd[None, :, None]).reshape(chunk.shape)
+    return y * g + b

@@ -151,6 +151,21 @@ def test_bad_calls_return_codes_without_a_gpu(lib):
     assert conv(3, rows, 16, 64, 128, 3, shards, good, None, outs, 2, None) == -3
     assert conv(3, rows, 16, 64, 128, 3, shards, P(0x10004), None, outs, 1, None) == -4
     assert conv(3, rows, 16, 64, 128, 3, shards, good, P(0x10002), outs, 1, None) == -4
+    n = ctypes.c_size_t()
+    assert lib.st_group_norm_workspace_size(256, 32, ctypes.byref(n)) == 0 and n.value >= 2048 * 32 * 12
+    assert lib.st_group_norm_workspace_size(256, 32, None) == -1
+    assert lib.st_group_norm_workspace_size(96, 4, ctypes.byref(n)) == -8       # C not a power of two
+    assert lib.st_group_norm_workspace_size(256, 64, ctypes.byref(n)) == -8     # 4 channels per group
+    gn = lib.st_group_norm_sharded
+    ws = P(0x70000)
+    big = 1 << 30
+    assert gn(3, rows, 16, 256, 32, 1e-5, None, None, None, outs, 0, 1, ws, big, None) == -1
+    assert gn(3, rows, 16, 256, 32, 0.0, shards, None, None, outs, 0, 1, ws, big, None) == -8     # eps
+    assert gn(3, rows, 16, 256, 32, 1e-5, shards, None, None, outs, 4, 1, ws, big, None) == -8    # out_pad
+    assert gn(3, rows, 16, 256, 32, 1e-5, shards, None, None, outs, 0, 2, ws, big, None) == -3
+    assert gn(3, rows, 16, 256, 32, 1e-5, shards, None, None, outs, 0, 1, None, big, None) == -5
+    assert gn(3, rows, 16, 256, 32, 1e-5, shards, None, None, outs, 0, 1, ws, 64, None) == -5
+    assert gn(3, rows, 16, 256, 32, 1e-5, shards, P(0x10002), None, outs, 0, 1, ws, big, None) == -4
 
 
 def test_python_binding_refuses_cpu_tensors(lib):
