@@ -10,6 +10,7 @@ from ._lib import (  # noqa: F401
     load,
     st_attn_bwd,
     st_attn_fwd,
+    st_attn_fwd_host,
     st_attn_fwd_partials,
     st_attn_merge,
     st_attn_workspace_size,

@@ -39,6 +39,8 @@ PROTOTYPES = [
                              ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     ("st_attn_workspace_size", _I, [_P, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     ("st_attn_fwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P, _SZ, _P]),
+    ("st_attn_fwd_host", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                              _P, _P]),
     ("st_attn_fwd_noalloc", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P]),
     ("st_attn_fwd_partials", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P]),
     ("st_attn_merge", _I, [_I, _I, _I, _I64, _I, _P, _P, _P, _P, _I, _P]),
@@ -205,6 +207,40 @@ def st_attn_fwd(layout, q, k, v, causal=False, scale=0.0, out=None, lse=None, st
                               _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)),
            "st_attn_fwd")
     return out, lse
+
+
+def st_attn_fwd_host(layout, q_host, k_host, v_host, out_host, lse_host, dev, causal=False, scale=0.0,
+                     workspace=None, stream=None, copy_stream=None):
+    """st_attn_fwd from host buffers with the copies overlapped with compute
+    (bf16 only).  ``q_host``, ``k_host``, ``v_host``, ``out_host`` are CPU
+    [B,S,H,d] bf16 tensors (pinned for overlap), ``lse_host`` CPU [B,H,S]
+    fp32; ``dev`` is a dict of device staging tensors ``q``, ``k``, ``v``,
+    ``out`` (same shape) and ``lse``.  ``copy_stream`` (a torch.cuda.Stream
+    other than ``stream``) carries the copies; it is created when not given.
+    When ``stream`` completes, out_host and lse_host hold the results."""
+    B, S, H, d = _shape(q_host)
+    for t, n in ((q_host, "q_host"), (k_host, "k_host"), (v_host, "v_host"), (out_host, "out_host")):
+        if t.is_cuda or tuple(t.shape) != (B, S, H, d) or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CPU bf16 tensor of shape %s" % (n, (B, S, H, d)))
+    if lse_host.is_cuda or tuple(lse_host.shape) != (B, H, S) or lse_host.dtype != torch.float32 \
+            or not lse_host.is_contiguous():
+        raise ValueError("lse_host must be a contiguous CPU fp32 tensor of shape %s" % ((B, H, S),))
+    for n in ("q", "k", "v", "out"):
+        _check_tensor(dev[n], (B, S, H, d), torch.bfloat16, n)
+    _check_tensor(dev["lse"], (B, H, S), torch.float32, "lse")
+    if workspace is None:
+        need = st_attn_workspace_size(layout, B, H, d, torch.bfloat16, 0)
+        workspace = torch.empty(max(need, 1), device=dev["q"].device, dtype=torch.uint8)
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if copy_stream is None:
+        copy_stream = torch.cuda.Stream(device=dev["q"].device)
+    _check(load().st_attn_fwd_host(layout.handle, B, H, d, ST_DTYPE_BF16, int(bool(causal)), float(scale),
+                                   _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(out_host), _ptr(lse_host),
+                                   _ptr(dev["q"]), _ptr(dev["k"]), _ptr(dev["v"]), _ptr(dev["out"]),
+                                   _ptr(dev["lse"]), _ptr(workspace), workspace.numel(), _stream(stream),
+                                   _stream(copy_stream)), "st_attn_fwd_host")
+    return out_host, lse_host
 
 
 def st_attn_fwd_partials(layout, q, k, v, causal=False, scale=0.0, stream=None):

@@ -6,6 +6,9 @@
 
 #include <cuda_runtime_api.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "common.h"
 
 namespace {
@@ -242,6 +245,117 @@ extern "C" int st_attn_fwd(const st_layout_t* L, int B, int H, int d, int dtype,
     st::SegTable t;
     st::fill_segtable(*L, 64, &t);
     return cuda_status(st::launch_fwd_simt(t, a, dtype, stream));
+}
+
+extern "C" int st_attn_fwd_host(const st_layout_t* L, int B, int H, int d, int dtype, int causal, float scale,
+                                const void* q_host, const void* k_host, const void* v_host, void* out_host,
+                                float* lse_host, void* q, void* k, void* v, void* out, float* lse,
+                                void* workspace, size_t ws_bytes, void* stream, void* copy_stream) {
+    int rc = check_common(L, B, H, d, dtype, &scale);
+    if (rc != ST_OK) return rc;
+    if (dtype != ST_DTYPE_BF16) return ST_ERR_UNSUPPORTED;
+    if (!q_host || !k_host || !v_host || !out_host || !lse_host || !q || !k || !v || !out || !lse)
+        return ST_ERR_NULL;
+    if (!copy_stream || copy_stream == stream) return ST_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+        return ST_ERR_MISALIGNED;
+    const int64_t S = L->S;
+    const int64_t rows = (int64_t)B * S * H;
+    const size_t need = st::fwd_workspace_bytes(rows, d, dtype);
+    if (!workspace || ws_bytes < need) return ST_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ST_ERR_MISALIGNED;
+
+    // Query tiles (256 rows of one segment each, in buffer order) and the
+    // buffer rows they start at.
+    st::SegTable t;
+    const int tile_rows = st::fwd_tc_tile_rows();
+    st::fill_segtable(*L, tile_rows, &t);
+    auto tile_row = [&](int tl) -> int64_t {   // first buffer row of tile tl (tl == ntiles: S)
+        if (tl >= t.ntiles) return S;
+        int sgm = 0;
+        while (t.seg_tile[sgm + 1] <= tl) ++sgm;
+        return t.seg_buf[sgm] + (int64_t)(tl - t.seg_tile[sgm]) * tile_rows;
+    };
+    // Chunks of query tiles: a short first chunk (about two waves of CTAs) so
+    // that compute starts early while the rest of Q arrives, a short last
+    // chunk so that little output is left to copy back after compute ends, and
+    // the bulk in between (whole waves where possible).
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int per_tile = B * H;                          // CTAs per query tile
+    const int edge = std::max(1, (2 * std::max(sms, 1) + per_tile - 1) / per_tile);
+    std::vector<int> cuts{0};
+    if (t.ntiles > 4 * edge) {
+        cuts.push_back(edge);
+        cuts.push_back(t.ntiles - edge);
+    }
+    cuts.push_back(t.ntiles);
+    const int nchunks = (int)cuts.size() - 1;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
+    std::vector<cudaEvent_t> ev(1 + 2 * nchunks, nullptr);
+    for (auto& e : ev)
+        if ((rc = cuda_status((int)cudaEventCreateWithFlags(&e, cudaEventDisableTiming))) != ST_OK) break;
+    auto finish = [&](int code) {
+        for (auto& e : ev)
+            if (e) cudaEventDestroy(e);   // released once pending work has passed it
+        return code;
+    };
+    if (rc != ST_OK) return finish(rc);
+    const size_t row_bytes = (size_t)H * d * 2;            // one token of q, k, v or out (bf16)
+    const size_t kv_bytes = (size_t)B * S * row_bytes;
+    auto ck = [&](cudaError_t e) { return cuda_status((int)e); };
+    // K and V first: every query tile needs all of them
+    if ((rc = ck(cudaMemcpyAsync(k, k_host, kv_bytes, cudaMemcpyHostToDevice, xs))) != ST_OK) return finish(rc);
+    if ((rc = ck(cudaMemcpyAsync(v, v_host, kv_bytes, cudaMemcpyHostToDevice, xs))) != ST_OK) return finish(rc);
+    if ((rc = ck(cudaEventRecord(ev[0], xs))) != ST_OK) return finish(rc);
+    for (int c = 0; c < nchunks; ++c) {
+        const int64_t r0 = tile_row(cuts[c]), r1 = tile_row(cuts[c + 1]);
+        for (int b = 0; b < B; ++b) {
+            const size_t off = ((size_t)b * S + r0) * row_bytes;
+            if ((rc = ck(cudaMemcpyAsync(static_cast<char*>(q) + off, static_cast<const char*>(q_host) + off,
+                                         (size_t)(r1 - r0) * row_bytes, cudaMemcpyHostToDevice, xs))) != ST_OK)
+                return finish(rc);
+        }
+        if ((rc = ck(cudaEventRecord(ev[1 + c], xs))) != ST_OK) return finish(rc);
+    }
+    // compute: the fp16 copy of V once K and V are in, then each chunk once its Q rows are in
+    st::AttnArgs a{q, k, v, out, lse, nullptr, nullptr, B, H, d, causal ? 1 : 0, scale, ST_DTYPE_BF16,
+                   nullptr, nullptr, nullptr};
+    char* ws = static_cast<char*>(workspace);
+    a.v16 = ws;
+    a.amax_bits = reinterpret_cast<unsigned*>(ws + need - 256);
+    a.exps = reinterpret_cast<int*>(ws + need - 128);
+    if ((rc = ck(cudaStreamWaitEvent(cs, ev[0], 0))) != ST_OK) return finish(rc);
+    if ((rc = cuda_status(st::launch_fp16_copy1(v, a.v16, rows * d, a.amax_bits, a.exps, stream))) != ST_OK)
+        return finish(rc);
+    for (int c = 0; c < nchunks; ++c) {
+        if ((rc = ck(cudaStreamWaitEvent(cs, ev[1 + c], 0))) != ST_OK) return finish(rc);
+        bool handled = false;
+        rc = st::launch_fwd_tc(*L, a, stream, &handled, cuts[c], cuts[c + 1]);
+        if (!handled) return finish(ST_ERR_UNSUPPORTED);
+        if ((rc = cuda_status(rc)) != ST_OK) return finish(rc);
+        if ((rc = ck(cudaEventRecord(ev[1 + nchunks + c], cs))) != ST_OK) return finish(rc);
+        // that chunk's output rows and lse back to the host while the next chunk runs
+        if ((rc = ck(cudaStreamWaitEvent(xs, ev[1 + nchunks + c], 0))) != ST_OK) return finish(rc);
+        const int64_t r0 = tile_row(cuts[c]), r1 = tile_row(cuts[c + 1]);
+        for (int b = 0; b < B; ++b) {
+            const size_t off = ((size_t)b * S + r0) * row_bytes;
+            if ((rc = ck(cudaMemcpyAsync(static_cast<char*>(out_host) + off, static_cast<const char*>(out) + off,
+                                         (size_t)(r1 - r0) * row_bytes, cudaMemcpyDeviceToHost, xs))) != ST_OK)
+                return finish(rc);
+        }
+        // lse [B, H, S]: rows r0 .. r1 of every (b, h)
+        if ((rc = ck(cudaMemcpy2DAsync(lse_host + r0, (size_t)S * 4, lse + r0, (size_t)S * 4, (size_t)(r1 - r0) * 4,
+                                       (size_t)B * H, cudaMemcpyDeviceToHost, xs))) != ST_OK)
+            return finish(rc);
+    }
+    // `stream` completes only after the last copy back
+    if ((rc = ck(cudaEventRecord(ev[0], xs))) != ST_OK) return finish(rc);
+    if ((rc = ck(cudaStreamWaitEvent(cs, ev[0], 0))) != ST_OK) return finish(rc);
+    return finish(ST_OK);
 }
 
 extern "C" int st_attn_fwd_partials(const st_layout_t* L, int B, int H, int d, int dtype,

@@ -100,7 +100,9 @@ BwdWorkspace bwd_workspace_layout(int64_t rows, int d, int dtype);
 
 // ---- launchers (return a cudaError_t value; 0 = success) ----
 int launch_fwd_simt(const SegTable& t, const AttnArgs& a, int dtype, void* stream);
-int launch_fwd_tc(const st_layout& L, const AttnArgs& a, void* stream, bool* handled);
+// Query tiles [t0, t1) of the layout's 256-row tiles (t1 < 0: all of them).
+int launch_fwd_tc(const st_layout& L, const AttnArgs& a, void* stream, bool* handled, int t0 = 0, int t1 = -1);
+int fwd_tc_tile_rows();
 int launch_bwd_simt(const SegTable& t, const BwdArgs& a, int dtype, void* stream);
 int launch_bwd_tc(const st_layout& L, const BwdArgs& a, void* stream, bool* handled);
 // Device error word of the tensor-core kernels (1 after a bounded wait gave

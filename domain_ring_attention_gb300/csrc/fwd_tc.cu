@@ -114,6 +114,7 @@ struct FwdParams {
     int out_f32;
     const int* exps;           // exps[0]: v16 = v * 2^-exps[0]
     int use_order;             // causal: CTAs take tiles heaviest first
+    int tile0;                 // first query tile of this launch (without an order)
     uint16_t order[kMaxOrder];
 };
 
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = p.H;
     const int b = blockIdx.y / H, h = blockIdx.y % H;
-    const int tile = p.use_order ? (int)p.order[blockIdx.x] : (int)blockIdx.x;
+    const int tile = p.use_order ? (int)p.order[blockIdx.x] : p.tile0 + (int)blockIdx.x;
     const QTile qt = locate_qtile(p.tab, tile, kNQ * kM);
     int nq_h[kNQ], nat_h[kNQ];
 #pragma unroll
@@ -681,7 +682,7 @@ bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int d,
 }
 
 template <int D, bool kSplit>
-int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
+int launch_t(const st_layout& L, const AttnArgs& a, void* stream, int t0, int t1) {
     using C = Cfg<D>;
     FwdParams p;
     const int S = (int)L.S;
@@ -689,16 +690,21 @@ int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
         !make_map(&p.tv, a.v16, a.B, S, a.H, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
         return (int)cudaErrorInvalidValue;
     fill_segtable(L, kNQ * kM, &p.tab);
+    if (t1 < 0 || t1 > p.tab.ntiles) t1 = p.tab.ntiles;
+    if (t0 < 0) t0 = 0;
+    if (t0 >= t1) return 0;
+    p.tile0 = t0;
     // Longest-processing-time-first order for causal work: a 256-row unit
     // ending at natural position e sees about e keys.  Units of one head are
     // issued heaviest first; heads stay in order (grid y) for L2 reuse of K/V.
     p.use_order = 0;
-    if (a.causal && p.tab.ntiles <= kMaxOrder) {
+    if (a.causal && t1 - t0 <= kMaxOrder) {
         std::vector<std::pair<int, int>> w;
         w.reserve(p.tab.ntiles);
         for (int s = 0; s < p.tab.nseg; ++s) {
             const int len = p.tab.seg_buf[s + 1] - p.tab.seg_buf[s];
             for (int tl = p.tab.seg_tile[s]; tl < p.tab.seg_tile[s + 1]; ++tl) {
+                if (tl < t0 || tl >= t1) continue;
                 const int local = (tl - p.tab.seg_tile[s]) * kNQ * kM;
                 const int nq = std::min(kNQ * kM, len - local);
                 w.emplace_back(-(p.tab.seg_nat[s] + local + nq), tl);
@@ -706,7 +712,7 @@ int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
         }
         std::stable_sort(w.begin(), w.end(),
                          [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first < y.first; });
-        for (int i = 0; i < p.tab.ntiles; ++i) p.order[i] = (uint16_t)w[i].second;
+        for (int i = 0; i < t1 - t0; ++i) p.order[i] = (uint16_t)w[i].second;
         p.use_order = 1;
     }
     p.q = a.q;
@@ -721,22 +727,24 @@ int launch_t(const st_layout& L, const AttnArgs& a, void* stream) {
     auto kern = fwd_tc_kernel<D, kSplit>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return (int)e;
-    dim3 grid(p.tab.ntiles, a.B * a.H);
+    dim3 grid(t1 - t0, a.B * a.H);
     kern<<<grid, kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
     return (int)cudaGetLastError();
 }
 
 }  // namespace
 
-int launch_fwd_tc(const st_layout& L, const AttnArgs& a, void* stream, bool* handled) {
+int fwd_tc_tile_rows() { return kNQ * kM; }
+
+int launch_fwd_tc(const st_layout& L, const AttnArgs& a, void* stream, bool* handled, int t0, int t1) {
     *handled = true;
     // partial tiles exist under causal masking or when a segment is not a
     // multiple of the 128-row tile
     bool split = a.causal != 0;
     for (size_t s = 0; s + 1 < L.seg_buf.size(); ++s)
         split |= ((L.seg_buf[s + 1] - L.seg_buf[s]) % kN) != 0;
-    if (a.d == 64) return split ? launch_t<64, true>(L, a, stream) : launch_t<64, false>(L, a, stream);
-    return split ? launch_t<128, true>(L, a, stream) : launch_t<128, false>(L, a, stream);
+    if (a.d == 64) return split ? launch_t<64, true>(L, a, stream, t0, t1) : launch_t<64, false>(L, a, stream, t0, t1);
+    return split ? launch_t<128, true>(L, a, stream, t0, t1) : launch_t<128, false>(L, a, stream, t0, t1);
 }
 
 int fwd_tc_device_error(bool clear) {

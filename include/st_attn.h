@@ -119,6 +119,33 @@ int st_attn_fwd(const st_layout_t* layout, int B, int H, int d, int dtype, int c
                 float scale, const void* q, const void* k, const void* v, int out_dtype,
                 void* out, float* lse, void* workspace, size_t ws_bytes, void* stream);
 
+/* Forward from host buffers, with the copies overlapped with the compute.
+ * It computes what st_attn_fwd computes (bf16 in, bf16 out) for inputs and
+ * outputs in host memory, and the outputs are bit for bit the same.
+ *   q_host, k_host, v_host : host [B,S,H,d] bf16 (page-locked memory lets
+ *                            the copies overlap the compute).
+ *   out_host : host [B,S,H,d] bf16;  lse_host : host [B,H,S] fp32.
+ *   q, k, v, out, lse      : device buffers of the same shapes, owned by
+ *                            the caller, used as the staging copies.
+ *   workspace, ws_bytes    : as st_attn_fwd (pass 0).
+ *   copy_stream            : a second stream, distinct from `stream`, that
+ *                            carries the copies.
+ * Order of work:
+ *   1. K and V are copied in on copy_stream; every query tile needs all of them.
+ *   2. Q follows on copy_stream in three chunks of query tiles: a short first
+ *      chunk (about two waves of CTAs), the bulk, and a short last chunk.
+ *   3. Each chunk is computed on `stream` as soon as its rows have arrived.
+ *   4. Its output rows and lse go back on copy_stream while the next chunk
+ *      computes.
+ * When `stream` has completed, every output is in host memory.  A few CUDA
+ * events are created and released per call; no device memory is allocated.
+ * Errors: as st_attn_fwd, plus ST_ERR_UNSUPPORTED for dtype other than bf16
+ * and ST_ERR_INVALID_ARG when copy_stream is NULL or equal to stream. */
+int st_attn_fwd_host(const st_layout_t* layout, int B, int H, int d, int dtype, int causal, float scale,
+                     const void* q_host, const void* k_host, const void* v_host, void* out_host, float* lse_host,
+                     void* q, void* k, void* v, void* out, float* lse, void* workspace, size_t ws_bytes,
+                     void* stream, void* copy_stream);
+
 /* Forward for callers that cannot allocate device memory.  No passage of the
  * paper corresponds to it: it is an interface for callers that are handed
  * only their input and output buffers (an operator running inside another

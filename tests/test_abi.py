@@ -105,6 +105,16 @@ def test_bad_calls_return_codes_without_a_gpu(lib):
     assert bwd(lay.handle, 1, 1, 64, 1, 0, 0.0, *qkv, good, 1, lse, good, 1, good, good, good, good, 16, None) == -5
     assert bwd(lay.handle, 1, 1, 64, 0, 0, 0.0, *qkv, good, 0, lse, good, 1, good, good, good, good, 1 << 30, None) == -3
     assert bwd(lay.handle, 1, 1, 64, 0, 0, 0.0, *qkv, good, 1, lse, good, 0, good, good, good, good, 1 << 30, None) == -3
+    fh = lib.st_attn_fwd_host
+    h5 = [good] * 5
+    d5 = [good, good, good, good, lse]
+    assert fh(lay.handle, 1, 1, 64, 1, 0, 0.0, None, good, good, good, lse, *d5, good, 1 << 30, None, good) == -1
+    assert fh(lay.handle, 1, 1, 64, 1, 0, 0.0, *h5, good, good, None, good, lse, good, 1 << 30, None, good) == -1
+    assert fh(lay.handle, 1, 1, 64, 1, 0, 0.0, *h5, *d5, good, 1 << 30, None, None) == -8    # no copy stream
+    assert fh(lay.handle, 1, 1, 64, 1, 0, 0.0, *h5, *d5, good, 1 << 30, good, good) == -8    # the same stream
+    assert fh(lay.handle, 1, 1, 64, 0, 0, 0.0, *h5, *d5, good, 1 << 30, None, good) == -3    # fp32
+    assert fh(lay.handle, 1, 1, 64, 1, 0, 0.0, *h5, *d5, good, 16, None, good) == -5          # workspace
+    assert fh(lay.handle, 1, 1, 64, 1, 0, 0.0, *h5, P(0x10004), *d5[1:], good, 1 << 30, None, good) == -4
     mrg = lib.st_attn_merge
     assert mrg(0, 1, 1, 64, 64, good, good, good, lse, 0, None) == -8
     assert mrg(33, 1, 1, 64, 64, good, good, good, lse, 0, None) == -8

@@ -1,0 +1,49 @@
+"""GPU checks of the host-buffer forward (st_attn_fwd_host).
+
+It must give, bit for bit, what st_attn_fwd gives on the same inputs: the same kernels on the same tiles, only
+launched per chunk of query tiles with the copies overlapped. The cases:
+- one chunk (few tiles);
+- three chunks (B * H = 64 CTAs per query tile);
+- causal zigzag over uneven shards, where the tile order inside each chunk is heaviest first.
+A few rows are also held to the oracle with the bf16 bounds.
+"""
+import numpy as np
+import pytest
+import torch
+
+import domain_ring_attention_gb300 as st
+from domain_ring_attention_gb300.workloads import Workload, make_inputs
+from oracle import attention as oa
+from gpu_common import assert_no_device_error, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("B,H,d,lens,causal,zigzag", [
+    (1, 4, 64, (512,) * 8, False, False),              # one chunk
+    (2, 32, 64, (1024,) * 8, False, False),            # three chunks: 5 + 22 + 5 tiles
+    (2, 32, 128, (2560, 1536, 3328, 768), True, True),  # three chunks, causal zigzag, uneven shards
+])
+def test_host_forward_equals_device_forward(B, H, d, lens, causal, zigzag):
+    wl = Workload("host", B=B, H=H, d=d, lens=lens, causal=causal, zigzag=zigzag, dtype="bf16")
+    q, k, v = make_inputs(wl, seed=3)
+    lay = st.Layout(lens, zigzag=zigzag)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    ref_out, ref_lse = st.st_attn_fwd(lay, qd, kd, vd, causal=causal)
+    pin = [x.pin_memory() for x in (q, k, v)]
+    out_h = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
+    lse_h = torch.empty(tuple(ref_lse.shape), dtype=torch.float32, pin_memory=True)
+    dev = {"q": torch.empty_like(qd), "k": torch.empty_like(kd), "v": torch.empty_like(vd),
+           "out": torch.empty_like(qd), "lse": torch.empty_like(ref_lse)}
+    st.st_attn_fwd_host(lay, pin[0], pin[1], pin[2], out_h, lse_h, dev, causal=causal)
+    torch.cuda.current_stream().synchronize()
+    assert_no_device_error()
+    assert torch.equal(out_h, ref_out.cpu())
+    assert torch.equal(lse_h, ref_lse.cpu())
+    # a few rows against the oracle: the first query row of every shard, for head 0 of batch 0
+    rows = np.cumsum((0,) + lens[:-1])
+    outs, lses = oa.forward_rows(f64(q), f64(k), f64(v), lens, zigzag, causal, rows, heads=[(0, 0)])
+    o, l = outs[(0, 0)], lses[(0, 0)]
+    err = np.abs(f64(out_h[0, rows, 0]) - o)
+    assert err.max() <= 1e-2, err.max()
+    assert np.abs(f64(lse_h[0, 0, rows]) - l).max() <= 1e-2
