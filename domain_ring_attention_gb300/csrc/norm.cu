@@ -13,8 +13,8 @@
 //                      deviations (M2) of the values it reads (every thread
 //                      keeps sums shifted by its first value, in fp32, then
 //                      the block merges its threads by the pairwise rule);
-//   gn_combine_kernel  the all-reduce: one block per group merges the blocks'
-//                      statistics by the pairwise rule in fp64 -> mean, 1/std;
+//   gn_combine_kernel  the all-reduce: one block per group adds up the blocks'
+//                      statistics as fp64 sums -> mean, 1/std;
 //   gn_apply_kernel    y = (x - mean) * (gamma / std) + beta, bf16 or fp32,
 //                      walked in the opposite order to the statistics pass so
 //                      that the rows read last there are still in L2.
@@ -125,32 +125,38 @@ __global__ void __launch_bounds__(kGnThreads) gn_stats_kernel(const __grid_const
     }
 }
 
-// one block per group: the all-reduce of the blocks' statistics, in fp64
+// one block per group: the all-reduce of the blocks' statistics.  In fp64
+// the pairwise rule needs a division per merge, which is slow; plain sums of
+// n, n*mean and M2 + n*mean^2 need none, and the one subtraction left at the
+// end (E[x^2] - mean^2) loses nothing that matters in 53 bits unless the mean
+// is beyond about 1e5 standard deviations.
 __global__ void __launch_bounds__(kGnThreads) gn_combine_kernel(const __grid_constant__ GnParams p) {
-    __shared__ double sn[kGnThreads], smean[kGnThreads], sm2[kGnThreads];
+    __shared__ double sn[kGnThreads], s1[kGnThreads], s2[kGnThreads];
     const int g = blockIdx.x;
-    double n = 0.0, m = 0.0, q = 0.0;
+    double n = 0.0, a = 0.0, q = 0.0;
     for (int b = threadIdx.x; b < p.nblocks; b += kGnThreads) {
         const float* src = p.partial + ((int64_t)b * p.G + g) * 3;
-        merge(n, m, q, (double)src[0], (double)src[1], (double)src[2]);
+        const double nb = src[0], mb = src[1];
+        n += nb;
+        a += nb * mb;
+        q += (double)src[2] + nb * mb * mb;
     }
     sn[threadIdx.x] = n;
-    smean[threadIdx.x] = m;
-    sm2[threadIdx.x] = q;
+    s1[threadIdx.x] = a;
+    s2[threadIdx.x] = q;
     __syncthreads();
     for (int h = kGnThreads / 2; h > 0; h >>= 1) {
         if (threadIdx.x < h) {
-            double a = sn[threadIdx.x], am = smean[threadIdx.x], aq = sm2[threadIdx.x];
-            merge(a, am, aq, sn[threadIdx.x + h], smean[threadIdx.x + h], sm2[threadIdx.x + h]);
-            sn[threadIdx.x] = a;
-            smean[threadIdx.x] = am;
-            sm2[threadIdx.x] = aq;
+            sn[threadIdx.x] += sn[threadIdx.x + h];
+            s1[threadIdx.x] += s1[threadIdx.x + h];
+            s2[threadIdx.x] += s2[threadIdx.x + h];
         }
         __syncthreads();
     }
     if (threadIdx.x == 0) {
-        const double var = sn[0] > 0.0 ? sm2[0] / sn[0] : 0.0;
-        p.stats[2 * g] = smean[0];
+        const double mean = sn[0] > 0.0 ? s1[0] / sn[0] : 0.0;
+        const double var = sn[0] > 0.0 ? fmax(s2[0] / sn[0] - mean * mean, 0.0) : 0.0;
+        p.stats[2 * g] = mean;
         p.stats[2 * g + 1] = 1.0 / sqrt(var + (double)p.eps);
     }
 }
@@ -160,7 +166,7 @@ __device__ __forceinline__ uint32_t pack_bf16_pair(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__global__ void __launch_bounds__(kGnThreads) gn_apply_kernel(const __grid_constant__ GnParams p) {
+__global__ void __launch_bounds__(kGnThreads, 4) gn_apply_kernel(const __grid_constant__ GnParams p) {
     const int vpp = 1 << p.vshift;
     const int64_t total = p.pix_off[p.D] << p.vshift;
     const int64_t stride = (int64_t)gridDim.x * kGnThreads;
@@ -268,15 +274,23 @@ int launch_group_norm(int D, const int64_t* rows, int W, int C, int G, float eps
     p.partial = static_cast<float*>(workspace);
     p.stats = reinterpret_cast<double*>(static_cast<char*>(workspace) +
                                         ((size_t)kGnStatBlocks * G * 3 * sizeof(float) + 255) / 256 * 256);
+    // grid-stride kernels: as many blocks as are resident at once (one wave)
     const int64_t vecs = p.pix_off[D] << p.vshift;
-    int64_t blocks = (vecs + kGnThreads - 1) / kGnThreads;
-    const int64_t cap = (int64_t)sm_count() * 8 < kGnStatBlocks ? (int64_t)sm_count() * 8 : kGnStatBlocks;
-    if (blocks > cap) blocks = cap;
-    p.nblocks = (int)blocks;
+    const int64_t want = (vecs + kGnThreads - 1) / kGnThreads;
+    auto wave = [&](const void* fn) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kGnThreads, 0) != cudaSuccess || per_sm < 1)
+            per_sm = 1;
+        int64_t n = (int64_t)sm_count() * per_sm;
+        if (n > kGnStatBlocks) n = kGnStatBlocks;
+        return (int)(want < n ? want : n);
+    };
+    p.nblocks = wave(reinterpret_cast<const void*>(gn_stats_kernel));
+    const int apply_blocks = wave(reinterpret_cast<const void*>(gn_apply_kernel));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     gn_stats_kernel<<<p.nblocks, kGnThreads, 0, s>>>(p);
     gn_combine_kernel<<<G, kGnThreads, 0, s>>>(p);
-    gn_apply_kernel<<<p.nblocks, kGnThreads, 0, s>>>(p);
+    gn_apply_kernel<<<apply_blocks, kGnThreads, 0, s>>>(p);
     return (int)cudaGetLastError();
 }
 
