@@ -307,10 +307,11 @@ extern "C" int st_attn_fwd_host(const st_layout_t* L, int B, int H, int d, int d
     const size_t row_bytes = (size_t)H * d * 2;            // one token of q, k, v or out (bf16)
     const size_t kv_bytes = (size_t)B * S * row_bytes;
     auto ck = [&](cudaError_t e) { return cuda_status((int)e); };
-    // K and V first: every query tile needs all of them
-    if ((rc = ck(cudaMemcpyAsync(k, k_host, kv_bytes, cudaMemcpyHostToDevice, xs))) != ST_OK) return finish(rc);
+    // V, then K: every query tile needs all of both; the fp16 copy of V runs
+    // while K is still coming in
     if ((rc = ck(cudaMemcpyAsync(v, v_host, kv_bytes, cudaMemcpyHostToDevice, xs))) != ST_OK) return finish(rc);
     if ((rc = ck(cudaEventRecord(ev[0], xs))) != ST_OK) return finish(rc);
+    if ((rc = ck(cudaMemcpyAsync(k, k_host, kv_bytes, cudaMemcpyHostToDevice, xs))) != ST_OK) return finish(rc);
     for (int c = 0; c < nchunks; ++c) {
         const int64_t r0 = tile_row(cuts[c]), r1 = tile_row(cuts[c + 1]);
         for (int b = 0; b < B; ++b) {
@@ -321,7 +322,8 @@ extern "C" int st_attn_fwd_host(const st_layout_t* L, int B, int H, int d, int d
         }
         if ((rc = ck(cudaEventRecord(ev[1 + c], xs))) != ST_OK) return finish(rc);
     }
-    // compute: the fp16 copy of V once K and V are in, then each chunk once its Q rows are in
+    // compute: the fp16 copy of V once V is in, then each chunk once its Q rows
+    // are in (they follow K on the copy stream)
     st::AttnArgs a{q, k, v, out, lse, nullptr, nullptr, B, H, d, causal ? 1 : 0, scale, ST_DTYPE_BF16,
                    nullptr, nullptr, nullptr};
     char* ws = static_cast<char*>(workspace);

@@ -131,7 +131,8 @@ int st_attn_fwd(const st_layout_t* layout, int B, int H, int d, int dtype, int c
  *   copy_stream            : a second stream, distinct from `stream`, that
  *                            carries the copies.
  * Order of work:
- *   1. K and V are copied in on copy_stream; every query tile needs all of them.
+ *   1. V, then K, are copied in on copy_stream; every query tile needs all of
+ *      them.  The fp16 copy of V runs on `stream` while K arrives.
  *   2. Q follows on copy_stream in three chunks of query tiles: a short first
  *      chunk (about two waves of CTAs), the bulk, and a short last chunk.
  *   3. Each chunk is computed on `stream` as soon as its rows have arrived.
