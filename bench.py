@@ -41,8 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 # workload, from the committed ncu capture of the kernel version named here
 # (2-head capture scaled by 8 to 16 heads: the traffic is per head); a kernel
 # change without a new capture must drop its entry (traffic is then null).
-NCU_TRAFFIC_BYTES = {"fwd_tc@ab29c69": 8 * (50.498304e6 + 1.126400e6)}
-KERNEL_VERSION = "fwd_tc@ab29c69"
+NCU_TRAFFIC_BYTES = {"fwd_tc@5875d80": 8 * (50.388224e6 + 0.517888e6)}
+KERNEL_VERSION = "fwd_tc@5875d80"
 DEFAULT_WORKLOAD = "vit4096_s65536"
 
 
