@@ -24,6 +24,7 @@ ERRORS = {
     0: "ST_OK", -1: "ST_ERR_NULL", -2: "ST_ERR_INVALID_LAYOUT", -3: "ST_ERR_UNSUPPORTED",
     -4: "ST_ERR_MISALIGNED", -5: "ST_ERR_WORKSPACE", -6: "ST_ERR_CUDA",
     -7: "ST_ERR_DEVICE_TIMEOUT", -8: "ST_ERR_INVALID_ARG", -9: "ST_ERR_SCRATCH_LIMIT",
+    -10: "ST_ERR_NOT_DEVICE",
 }
 
 # C prototypes: (name, restype, argtypes)
@@ -48,6 +49,7 @@ PROTOTYPES = [
                          _P, _SZ, _P]),
     ("st_permute", _I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     ("st_proj_gemm", _I, [_I, _I, _I, _P, _P, _P, _I, _P]),
+    ("st_is_device_pointer", _I, [_P]),
     ("st_gated_mlp", _I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
     ("st_halo_exchange", _I, [_I, ctypes.POINTER(_I64), _I, _I, _I, ctypes.POINTER(_P), _P]),
     ("st_conv2d_sharded", _I, [_I, ctypes.POINTER(_I64), _I, _I, _I, _I, ctypes.POINTER(_P), _P, _P,

@@ -23,6 +23,32 @@ int cuda_status(int err) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Memory the kernels may read and write: device or managed allocations.  A
+// pointer to ordinary host memory handed to a kernel would fault the GPU, so
+// every entry point checks its device pointers with the runtime, after all its
+// other checks (so argument errors are still reported without a GPU).  NULL
+// is accepted here (optional arguments were checked before).
+bool on_device(const void* p) {
+    if (!p) return true;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();   // do not leave the failure to be read as a launch error
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+template <typename... P>
+bool all_on_device(P... ps) {
+    return (on_device(ps) && ...);
+}
+
+bool shards_on_device(int D, void* const* shards) {
+    for (int r = 0; r < D; ++r)
+        if (!on_device(shards[r])) return false;
+    return true;
+}
+
 int check_common(const st_layout_t* L, int B, int H, int d, int dtype, float* scale) {
     if (!L) return ST_ERR_NULL;
     if (B < 1 || H < 1 || (int64_t)B * H > 65535) return ST_ERR_INVALID_ARG;
@@ -47,11 +73,14 @@ extern "C" const char* st_error_string(int code) {
         case ST_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
         case ST_ERR_INVALID_ARG: return "an argument is out of range";
         case ST_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed 32 MiB scratch of st_attn_fwd_noalloc";
+        case ST_ERR_NOT_DEVICE: return "a pointer that must address device memory does not";
         default: return "unknown status";
     }
 }
 
 extern "C" int st_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" int st_is_device_pointer(const void* p) { return p && on_device(p) ? 1 : 0; }
 
 extern "C" int st_device_error(void* stream) {
     int rc = cuda_status((int)cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
@@ -70,6 +99,7 @@ extern "C" int st_proj_gemm(int M, int N, int K, const void* x, const void* w, v
     if (M < 1 || N < 1 || K < 1 || N % 8 != 0 || K % 8 != 0) return ST_ERR_INVALID_ARG;
     if (out_dtype != ST_DTYPE_BF16 && out_dtype != ST_DTYPE_F32) return ST_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return ST_ERR_MISALIGNED;
+    if (!all_on_device(x, w, y)) return ST_ERR_NOT_DEVICE;
     return cuda_status(st::launch_gemm_tc(M, N, K, x, w, y, out_dtype, stream));
 }
 
@@ -98,6 +128,7 @@ extern "C" int st_halo_exchange(int D, const int64_t* rows, int W, int C, int ha
     if (rc != ST_OK) return rc;
     if (C < 8 || C % 8 != 0 || halo < 0 || halo > 3) return ST_ERR_INVALID_ARG;
     if ((int64_t)W * C > (1 << 24)) return ST_ERR_INVALID_ARG;
+    if (!shards_on_device(D, shards)) return ST_ERR_NOT_DEVICE;
     return cuda_status(st::launch_halo_exchange(D, rows, W, C, halo, shards, stream));
 }
 
@@ -114,6 +145,8 @@ extern "C" int st_conv2d_sharded(int D, const int64_t* rows, int W, int C_in, in
         return ST_ERR_INVALID_ARG;
     if (out_dtype != ST_DTYPE_BF16 && out_dtype != ST_DTYPE_F32) return ST_ERR_UNSUPPORTED;
     if (!aligned16(weight) || (bias && reinterpret_cast<uintptr_t>(bias) % 4 != 0)) return ST_ERR_MISALIGNED;
+    if (!shards_on_device(D, in_shards) || !shards_on_device(D, out_shards) || !all_on_device(weight, bias))
+        return ST_ERR_NOT_DEVICE;
     return cuda_status(
         st::launch_conv_tc(D, rows, W, C_in, C_out, k, in_shards, weight, bias, out_shards, out_dtype, stream));
 }
@@ -154,6 +187,9 @@ extern "C" int st_group_norm_sharded(int D, const int64_t* rows, int W, int C, i
     if (!workspace) return ST_ERR_WORKSPACE;
     if (ws_bytes < st::group_norm_workspace_bytes(G)) return ST_ERR_WORKSPACE;
     if (!aligned16(workspace)) return ST_ERR_MISALIGNED;
+    if (!shards_on_device(D, const_cast<void* const*>(in_shards)) || !shards_on_device(D, out_shards) ||
+        !all_on_device(gamma, beta, workspace))
+        return ST_ERR_NOT_DEVICE;
     return cuda_status(st::launch_group_norm(D, rows, W, C, G, eps, in_shards, gamma, beta, out_shards, out_pad,
                                              out_dtype, workspace, stream));
 }
@@ -165,6 +201,7 @@ extern "C" int st_gated_mlp(int M, int hidden, int F, const void* x, const void*
     if (out_dtype != ST_DTYPE_BF16 && out_dtype != ST_DTYPE_F32) return ST_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) || !aligned16(h) || !aligned16(y))
         return ST_ERR_MISALIGNED;
+    if (!all_on_device(x, w1, w3, w2, h, y)) return ST_ERR_NOT_DEVICE;
     int rc = cuda_status(st::launch_gemm_gated(M, F, hidden, x, w1, w3, h, stream));
     if (rc != ST_OK) return rc;
     return cuda_status(st::launch_gemm_tc(M, hidden, F, h, w2, y, out_dtype, stream));
@@ -231,6 +268,7 @@ extern "C" int st_attn_fwd(const st_layout_t* L, int B, int H, int d, int dtype,
         const size_t need = st::fwd_workspace_bytes(rows, d, dtype);
         if (!workspace || ws_bytes < need) return ST_ERR_WORKSPACE;
         if (!aligned16(workspace)) return ST_ERR_MISALIGNED;
+        if (!all_on_device(q, k, v, out, lse, workspace)) return ST_ERR_NOT_DEVICE;
         char* ws = static_cast<char*>(workspace);
         a.v16 = ws;
         a.amax_bits = reinterpret_cast<unsigned*>(ws + need - 256);
@@ -242,6 +280,7 @@ extern "C" int st_attn_fwd(const st_layout_t* L, int B, int H, int d, int dtype,
         if (handled) return cuda_status(rc);
         return ST_ERR_UNSUPPORTED;
     }
+    if (!all_on_device(q, k, v, out, lse)) return ST_ERR_NOT_DEVICE;
     st::SegTable t;
     st::fill_segtable(*L, 64, &t);
     return cuda_status(st::launch_fwd_simt(t, a, dtype, stream));
@@ -264,6 +303,7 @@ extern "C" int st_attn_fwd_host(const st_layout_t* L, int B, int H, int d, int d
     const size_t need = st::fwd_workspace_bytes(rows, d, dtype);
     if (!workspace || ws_bytes < need) return ST_ERR_WORKSPACE;
     if (!aligned16(workspace)) return ST_ERR_MISALIGNED;
+    if (!all_on_device(q, k, v, out, lse, workspace)) return ST_ERR_NOT_DEVICE;
 
     // Query tiles (256 rows of one segment each, in buffer order) and the
     // buffer rows they start at.
@@ -372,6 +412,7 @@ extern "C" int st_attn_fwd_partials(const st_layout_t* L, int B, int H, int d, i
         return ST_ERR_MISALIGNED;
     st::AttnArgs a{q, k, v, nullptr, nullptr, partial_out, partial_lse, B, H, d, causal ? 1 : 0, scale,
                    ST_DTYPE_F32};
+    if (!all_on_device(q, k, v, partial_out, partial_lse)) return ST_ERR_NOT_DEVICE;
     st::SegTable t;
     st::fill_segtable(*L, 64, &t);
     return cuda_status(st::launch_fwd_simt(t, a, dtype, stream));
@@ -387,6 +428,7 @@ extern "C" int st_attn_merge(int D, int B, int H, int64_t S, int d, const float*
     if (out_dtype != ST_DTYPE_F32 && out_dtype != ST_DTYPE_BF16) return ST_ERR_UNSUPPORTED;
     if (!aligned16(partial_out) || !aligned16(partial_lse) || !aligned16(out) || !aligned16(lse))
         return ST_ERR_MISALIGNED;
+    if (!all_on_device(partial_out, partial_lse, out, lse)) return ST_ERR_NOT_DEVICE;
     return cuda_status(st::launch_merge(D, B, H, S, d, partial_out, partial_lse, out, lse,
                                         out_dtype, stream));
 }
@@ -408,6 +450,7 @@ extern "C" int st_attn_bwd(const st_layout_t* L, int B, int H, int d, int dtype,
     const st::BwdWorkspace w = st::bwd_workspace_layout(rows, d, dtype);
     if (!workspace || ws_bytes < w.total) return ST_ERR_WORKSPACE;
     if (!aligned16(workspace)) return ST_ERR_MISALIGNED;
+    if (!all_on_device(q, k, v, out, lse, dout, dq, dk, dv, workspace)) return ST_ERR_NOT_DEVICE;
     char* ws = static_cast<char*>(workspace);
     st::BwdArgs a{};
     a.q = q;
@@ -470,6 +513,7 @@ extern "C" int st_permute(const st_layout_t* L, int B, int H, int d, int dtype, 
     if (!in || !out) return ST_ERR_NULL;
     if (in == out) return ST_ERR_INVALID_ARG;
     if (!aligned16(in) || !aligned16(out)) return ST_ERR_MISALIGNED;
+    if (!all_on_device(in, out)) return ST_ERR_NOT_DEVICE;
     st::SegTable t;
     st::fill_segtable(*L, 64, &t);
     return cuda_status(st::launch_permute(t, B, H, d, dtype, to_natural ? 1 : 0, in, out, stream));

@@ -30,7 +30,10 @@
  *   - Pointers named q, k, ... are DEVICE pointers that the caller owns and
  *     keeps alive until the work on `stream` has finished; they must be
  *     16-byte aligned.  `stream` is a cudaStream_t (NULL = legacy default
- *     stream).  All GPU work is asynchronous on that stream.
+ *     stream).  All GPU work is asynchronous on that stream.  After every
+ *     other check, each call asks the CUDA runtime whether its device
+ *     pointers address device (or managed) memory and returns
+ *     ST_ERR_NOT_DEVICE if one does not, before anything is launched.
  *   - No call allocates device memory.  Scratch that a call needs is a
  *     caller-provided workspace whose size st_attn_workspace_size reports.
  *   - Every call returns ST_OK (0) or a negative ST_ERR_* code; no call aborts
@@ -57,7 +60,8 @@ enum {
     ST_ERR_CUDA = -6,            /* a CUDA runtime call or launch failed            */
     ST_ERR_DEVICE_TIMEOUT = -7,  /* a bounded device-side wait gave up              */
     ST_ERR_INVALID_ARG = -8,     /* B, H, S, D or another size is out of range      */
-    ST_ERR_SCRATCH_LIMIT = -9    /* problem too large for st_attn_fwd_noalloc       */
+    ST_ERR_SCRATCH_LIMIT = -9,   /* problem too large for st_attn_fwd_noalloc       */
+    ST_ERR_NOT_DEVICE = -10      /* a device-pointer argument is not device memory  */
 };
 
 enum { ST_DTYPE_F32 = 0, ST_DTYPE_BF16 = 1 };
@@ -388,6 +392,11 @@ int st_device_error(void* stream);
 
 /* Human-readable text for a status code (static storage). */
 const char* st_error_string(int code);
+
+/* 1 if p addresses device (or managed) memory, the check every entry point
+ * applies to its device pointers; 0 for NULL, host memory (page-locked or
+ * not) and addresses the runtime does not know.  Host only, never launches. */
+int st_is_device_pointer(const void* p);
 
 /* CUDA runtime error code behind the most recent ST_ERR_CUDA of this thread. */
 int st_last_cuda_error(void);
