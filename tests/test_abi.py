@@ -184,3 +184,28 @@ def test_python_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         st.st_attn_fwd(lay, x, x, x)
+
+
+def test_bindings_refuse_host_memory(lib):
+    """Every entry point checks, before it launches, that its device pointers address device memory: host
+    tensors come back as ST_ERR_NOT_DEVICE (no GPU is needed to see it)."""
+    import types
+    import torch
+    bf = torch.bfloat16
+    x = torch.zeros(64, 64, dtype=bf)
+    w = torch.zeros(64, 64, dtype=bf)
+    s0 = types.SimpleNamespace(cuda_stream=0)    # the legacy default stream, without asking torch for one
+    cases = [
+        lambda: st.st_proj_gemm(x, w, stream=s0),
+        lambda: st.st_gated_mlp(x, w, w, w, stream=s0),
+        lambda: st.st_halo_exchange([torch.zeros(6, 8, 64, dtype=bf), torch.zeros(5, 8, 64, dtype=bf)], 1, stream=s0),
+        lambda: st.st_conv2d_sharded([torch.zeros(6, 8, 64, dtype=bf)], torch.zeros(64, 3, 3, 64, dtype=bf),
+                                     stream=s0),
+        lambda: st.st_group_norm_sharded([torch.zeros(4, 8, 64, dtype=bf)], 8, stream=s0),
+    ]
+    for call in cases:
+        with pytest.raises(st.StAttnError) as e:
+            call()
+        assert e.value.code == -10, e.value
+    assert lib.st_is_device_pointer(ctypes.c_void_p(x.data_ptr())) == 0
+    assert lib.st_error_string(-10).decode().startswith("a pointer that must address device memory")
