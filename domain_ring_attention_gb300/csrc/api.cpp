@@ -43,6 +43,9 @@ bool all_on_device(P... ps) {
     return (on_device(ps) && ...);
 }
 
+// The GEMM kernels count output tiles (128 x 128 at the finest) in int.
+bool gemm_tiles_fit(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + 127) / 128) < ((int64_t)1 << 31); }
+
 bool shards_on_device(int D, void* const* shards) {
     for (int r = 0; r < D; ++r)
         if (!on_device(shards[r])) return false;
@@ -96,7 +99,7 @@ extern "C" int st_device_error(void* stream) {
 extern "C" int st_proj_gemm(int M, int N, int K, const void* x, const void* w, void* y, int out_dtype,
                             void* stream) {
     if (!x || !w || !y) return ST_ERR_NULL;
-    if (M < 1 || N < 1 || K < 1 || N % 8 != 0 || K % 8 != 0) return ST_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1 || N % 8 != 0 || K % 8 != 0 || !gemm_tiles_fit(M, N)) return ST_ERR_INVALID_ARG;
     if (out_dtype != ST_DTYPE_BF16 && out_dtype != ST_DTYPE_F32) return ST_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return ST_ERR_MISALIGNED;
     if (!all_on_device(x, w, y)) return ST_ERR_NOT_DEVICE;
@@ -143,6 +146,10 @@ extern "C" int st_conv2d_sharded(int D, const int64_t* rows, int W, int C_in, in
     if (k < 1 || k > 7 || k % 2 == 0 || C_in < 64 || C_in % 64 != 0 || C_in > 4096 || C_out < 8 ||
         C_out % 8 != 0 || C_out > 4096)
         return ST_ERR_INVALID_ARG;
+    int64_t H = 0;
+    for (int r = 0; r < D; ++r) H += rows[r];
+    // the kernel counts (row, 128-pixel tile, channel tile) units in int
+    if (H * ((W + 127) / 128) * ((C_out + 127) / 128) >= ((int64_t)1 << 31)) return ST_ERR_INVALID_ARG;
     if (out_dtype != ST_DTYPE_BF16 && out_dtype != ST_DTYPE_F32) return ST_ERR_UNSUPPORTED;
     if (!aligned16(weight) || (bias && reinterpret_cast<uintptr_t>(bias) % 4 != 0)) return ST_ERR_MISALIGNED;
     if (!shards_on_device(D, in_shards) || !shards_on_device(D, out_shards) || !all_on_device(weight, bias))
@@ -197,7 +204,9 @@ extern "C" int st_group_norm_sharded(int D, const int64_t* rows, int W, int C, i
 extern "C" int st_gated_mlp(int M, int hidden, int F, const void* x, const void* w1, const void* w3,
                             const void* w2, void* h, void* y, int out_dtype, void* stream) {
     if (!x || !w1 || !w3 || !w2 || !h || !y) return ST_ERR_NULL;
-    if (M < 1 || hidden < 1 || F < 1 || hidden % 8 != 0 || F % 8 != 0) return ST_ERR_INVALID_ARG;
+    if (M < 1 || hidden < 1 || F < 1 || hidden % 8 != 0 || F % 8 != 0 || !gemm_tiles_fit(M, F) ||
+        !gemm_tiles_fit(M, hidden))
+        return ST_ERR_INVALID_ARG;
     if (out_dtype != ST_DTYPE_BF16 && out_dtype != ST_DTYPE_F32) return ST_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) || !aligned16(h) || !aligned16(y))
         return ST_ERR_MISALIGNED;

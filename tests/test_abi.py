@@ -129,6 +129,7 @@ def test_bad_calls_return_codes_without_a_gpu(lib):
     assert gemm(64, 256, 60, good, good, good, 1, None) == -8      # K not a multiple of 8
     assert gemm(64, 256, 64, good, good, good, 2, None) == -3
     assert gemm(64, 256, 64, P(0x10004), good, good, 1, None) == -4
+    assert gemm(1 << 30, 1 << 20, 64, good, good, good, 1, None) == -8   # more output tiles than an int counts
     mlp = lib.st_gated_mlp
     w = [good] * 3
     assert mlp(64, 256, 512, None, *w, good, good, 1, None) == -1
@@ -161,6 +162,8 @@ def test_bad_calls_return_codes_without_a_gpu(lib):
     assert conv(3, rows, 16, 64, 128, 3, shards, good, None, outs, 2, None) == -3
     assert conv(3, rows, 16, 64, 128, 3, shards, P(0x10004), None, outs, 1, None) == -4
     assert conv(3, rows, 16, 64, 128, 3, shards, good, P(0x10002), outs, 1, None) == -4
+    assert conv(3, (ctypes.c_int64 * 3)(1 << 22, 1 << 22, 1 << 22), 1 << 20, 64, 128, 3, shards, good, None, outs,
+                1, None) == -8                                              # too many units for an int
     n = ctypes.c_size_t()
     assert lib.st_group_norm_workspace_size(256, 32, ctypes.byref(n)) == 0 and n.value >= 2048 * 32 * 12
     assert lib.st_group_norm_workspace_size(256, 32, None) == -1
