@@ -16,7 +16,7 @@
 //   dV  += P^T dO           (A = P^T from TMEM)
 //   dK  += dS^T Q           (A = dS^T, K-major view of the smem tile)
 //   dQ_t = dS K             (A = dS, MN-major view of the same smem tile)
-//   dQ  += scale dQ_t       (softmax warps: TMEM -> shared memory -> TMA bulk reduction)
+//   dQ  += scale dQ_t       (softmax warps: TMEM -> the dS^T lo tile -> TMA bulk reduction)
 //
 // Warp roles (384 threads): warp 0 TMA producer (+ lse / Delta staging),
 // warp 1 TMEM allocator + MMA issuer, warps 4-7 softmax for query columns
@@ -380,11 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const int natk = kt.nat0 + r;
         const float sl2 = ldexpf(p.scale_log2, p.exps[0] + p.exps[1]);    // S' -> scaled log2 units
         const float sc = ldexpf(p.scale, p.exps[4] + p.exps[1]);           // dQ_t -> dQ
-        // dQ staging: the 4 KB of the dS^T tile (and of its lo part) that this
-        // warp itself writes -- its 32 key rows of its group's 64 columns -- are
-        // free from the end of a tile's MMAs until its next softmax pass
-        const uint32_t stg0 = sS + (uint32_t)(grp * C::kChunkBytes + quad * 32 * 128);
-        const uint32_t stg1 = sS2 + (uint32_t)(grp * C::kChunkBytes + quad * 32 * 128);
+        // dQ staging: the 4 KB of the dS^T lo tile that this warp itself
+        // writes -- its 32 key rows of its group's 64 columns.  The lo tile is
+        // written only by the softmax passes of split tiles (partial tiles and
+        // the lead key tile), so the next pass of an ordinary tile need not
+        // wait for the TMA to have read the staged dQ out of it.
+        const uint32_t stg = sS2 + (uint32_t)(grp * C::kChunkBytes + quad * 32 * 128);
         // Write (or, after a flush, add) this key row's dV (group 0) or
         // scale * dK (group 1) from the TMEM accumulator into the output.
         auto emit = [&](bool have, bool add) {
@@ -533,7 +534,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             const bool row_ok = quad * 32 + lane < nq;
 #pragma unroll
             for (int c = 0; c < kCols / 32; ++c) {
-                const uint32_t buf = c == 0 ? stg0 : stg1;
+                // one staging slice: the TMA has read the previous chunk (or the
+                // previous tile's last chunk) out of it first
+                if (lane == 0) bulk_wait_read_0();
+                __syncwarp();
+                const uint32_t buf = stg;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     // 16-byte unit k of row `lane` under the 128-byte swizzle
@@ -547,9 +552,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 }
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) tma_reduce_add_4d(&p.tdq, buf, grp * kCols + c * 32, h, q0 + quad * 32, b);
+                if (lane == 0) {
+                    tma_reduce_add_4d(&p.tdq, buf, grp * kCols + c * 32, h, q0 + quad * 32, b);
+                    bulk_commit_group();
+                }
             }
-            if (lane == 0) bulk_commit_group();
         };
         int i = 0;
         bool ok = true;
@@ -567,13 +574,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_s, i & 1, abort_flag));
             if (!ok) return;
             tc_fence_after();
-            // the dQ tiles staged in this warp's part of the dS^T buffers have
-            // been read by the TMA before the softmax pass overwrites them
-            if (lane == 0) bulk_wait_read_0();
-            __syncwarp();
             // this stage's row statistics (shared-memory address)
             const uint32_t ls = sbase + C::kLOff + (uint32_t)(s * 2 * kT * 4);
             const int kind = classify(causal, natq, nq, kt.nat0, kt.nq, kT);
+            // a pass that writes the lo tile waits until the TMA has read the
+            // dQ staged in this warp's slice of it
+            if (kind == kPartial || lead_tile) {
+                if (lane == 0) bulk_wait_read_0();
+                __syncwarp();
+            }
             if (kind == kPartial) {
                 // causal: query column c sees key natk iff natk <= natq + c
                 const int cmin = causal ? max(0, natk - natq) : 0;
