@@ -33,6 +33,7 @@ lse_i) on visible pairs,
 from __future__ import annotations
 
 import math
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -310,3 +311,96 @@ def backward_rows(q, k, v, dout, lens, zigzag, causal, rows, scale=None, heads=N
         ds = p * (dp - delta[:, None])
         res[(b, h)] = scale * (ds @ k[b, :, h])
     return res
+
+
+def row_stats(q, k, v, dout, lens, zigzag=False, causal=False, scale=None, heads=None, workers=1,
+              block=256):
+    """out, lse and Delta_i = <dO_i, out_i> of every query row of the selected heads.
+
+    The definition again, for long sequences: blocks of query rows in natural
+    order, each scored against the keys it can see -- under causal masking a
+    block of natural rows [i0, i1) sees only natural keys 0 .. i1-1 (the
+    others would enter as exp(-inf) = 0) -- with the keys above a row's own
+    position masked inside the block.  Blocks hold independent rows; with
+    ``workers`` > 1 they run on a thread pool (numpy releases the interpreter
+    lock inside matmul and the elementwise steps).  ``block`` is the number of
+    query rows per block.
+    Returns three dicts keyed by (b, h): out [S, d], lse [S], delta [S], all in
+    buffer order.
+    """
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    B, S, H, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    pos = natural_positions(lens, zigzag)
+    order = np.argsort(pos, kind="stable")   # natural position -> buffer row
+    if heads is None:
+        heads = [(b, h) for b in range(B) for h in range(H)]
+    blk = int(block)
+    outs, lses, deltas = {}, {}, {}
+    for (b, h) in heads:
+        qn, kn, vn, don = q[b, order, h], k[b, order, h], v[b, order, h], dout[b, order, h]
+        on = np.zeros((S, d))
+        ln = np.zeros(S)
+        dn = np.zeros(S)
+
+        def block(i0):
+            i1 = min(S, i0 + blk)
+            n_keys = i1 if causal else S
+            s = scale * (qn[i0:i1] @ kn[:n_keys].T)
+            if causal:
+                rows = np.arange(i0, i1)[:, None]
+                s = np.where(np.arange(n_keys)[None, :] <= rows, s, NEG_INF)
+            l_blk, p = _softmax_rows(s)
+            o = p @ vn[:n_keys]
+            on[i0:i1] = o
+            ln[i0:i1] = l_blk
+            dn[i0:i1] = np.sum(don[i0:i1] * o, axis=1)
+
+        starts = list(range(0, S, blk))
+        if workers > 1:
+            with ThreadPoolExecutor(workers) as ex:
+                list(ex.map(block, starts))
+        else:
+            for i0 in starts:
+                block(i0)
+        out_b = np.empty_like(on)
+        out_b[order] = on
+        lse_b = np.empty_like(ln)
+        lse_b[order] = ln
+        delta_b = np.empty_like(dn)
+        delta_b[order] = dn
+        outs[(b, h)], lses[(b, h)], deltas[(b, h)] = out_b, lse_b, delta_b
+    return outs, lses, deltas
+
+
+def backward_cols(q, k, v, dout, lens, zigzag, causal, cols, lse, delta, scale=None, heads=None):
+    """dK and dV of selected key columns (buffer rows of k and v).
+
+    Over the queries i that see key j, with P_ij = exp(scale <q_i, k_j> - lse_i):
+        dV_j = sum_i P_ij dO_i,
+        dK_j = scale sum_i P_ij (<dO_i, v_j> - Delta_i) q_i.
+    ``lse`` and ``delta`` are dicts keyed by (b, h) holding every query row's
+    lse and Delta (buffer order), e.g. from ``row_stats``.  Returns two dicts
+    keyed by (b, h): dk [len(cols), d], dv [len(cols), d].
+    """
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    B, S, H, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    pos = natural_positions(lens, zigzag)
+    cols = np.asarray(cols, dtype=np.int64)
+    if heads is None:
+        heads = [(b, h) for b in range(B) for h in range(H)]
+    dks, dvs = {}, {}
+    for (b, h) in heads:
+        l_h = _as_f64(lse[(b, h)])
+        dl_h = _as_f64(delta[(b, h)])
+        s = scale * (q[b, :, h] @ k[b, cols, h].T)            # [S queries, n keys]
+        vis = _visible(pos, pos[cols], causal)
+        p = np.exp(np.where(vis, s - l_h[:, None], NEG_INF))
+        dp = dout[b, :, h] @ v[b, cols, h].T
+        ds = p * (dp - dl_h[:, None])
+        dvs[(b, h)] = p.T @ dout[b, :, h]
+        dks[(b, h)] = scale * (ds.T @ q[b, :, h])
+    return dks, dvs

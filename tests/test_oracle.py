@@ -362,3 +362,66 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     monkeypatch.undo()
     out_ok, _ = oa.forward(qb, qb, qb, lens, True, True)
     assert not np.allclose(out_bad, out_ok, atol=1e-6)
+
+
+# ---------------------------------------------------------------- long-sequence helpers
+
+def _natural_autograd(q, k, v, do, lens, zigzag, causal):
+    """torch SDPA and autograd in float64 on natural-order copies; results back in buffer order."""
+    pos = ol.natural_positions(lens, zigzag)
+    inv = np.argsort(pos)
+    ts = [torch.from_numpy(np.ascontiguousarray(x[:, inv])).permute(0, 2, 1, 3).requires_grad_()
+          for x in (q, k, v)]
+    o = torch.nn.functional.scaled_dot_product_attention(*ts, is_causal=causal)
+    o.backward(torch.from_numpy(np.ascontiguousarray(do[:, inv])).permute(0, 2, 1, 3))
+    back = lambda t: to_buffer(t.detach().permute(0, 2, 1, 3).numpy(), pos)
+    lse = torch_lse(np.ascontiguousarray(q[:, inv]), np.ascontiguousarray(k[:, inv]), causal,
+                    1 / math.sqrt(q.shape[-1]))
+    return back(o), lse[:, :, pos], [back(t.grad) for t in ts]
+
+
+@pytest.mark.parametrize("lens,zigzag,causal,workers", [
+    ([150, 50, 250, 150], True, True, 1), ([150, 50, 250, 150], True, True, 3),
+    ([301, 299], False, False, 2), ([600], False, True, 1)])
+def test_row_stats_match_torch(lens, zigzag, causal, workers):
+    S, d = sum(lens), 8
+    q, k, v, do = (rnd((1, S, 2, d), s) for s in (70, 71, 72, 73))
+    out_t, lse_t, _ = _natural_autograd(q, k, v, do, lens, zigzag, causal)
+    outs, lses, deltas = oa.row_stats(q, k, v, do, lens, zigzag, causal, workers=workers, block=128)
+    for (b, h), o in outs.items():
+        np.testing.assert_allclose(o, out_t[b, :, h], atol=1e-12)
+        np.testing.assert_allclose(lses[(b, h)], lse_t[b, h], atol=1e-12)
+        np.testing.assert_allclose(deltas[(b, h)], np.sum(do[b, :, h] * out_t[b, :, h], axis=1), atol=1e-11)
+
+
+@pytest.mark.parametrize("lens,zigzag,causal", [([150, 50, 250, 150], True, True), ([301, 299], False, False),
+                                                ([6, 2, 10, 4], True, True)])
+def test_backward_cols_match_torch_autograd(lens, zigzag, causal):
+    S, d = sum(lens), 8
+    q, k, v, do = (rnd((2, S, 2, d), s) for s in (80, 81, 82, 83))
+    _, _, (gq, gk, gv) = _natural_autograd(q, k, v, do, lens, zigzag, causal)
+    pos = ol.natural_positions(lens, zigzag)
+    # the key of the first natural position (seen by every query), the last one, and a spread
+    cols = np.unique(np.concatenate([[int(np.argmin(pos)), int(np.argmax(pos))], np.arange(0, S, 7)]))
+    _, lses, deltas = oa.row_stats(q, k, v, do, lens, zigzag, causal, block=64)
+    dks, dvs = oa.backward_cols(q, k, v, do, lens, zigzag, causal, cols, lses, deltas)
+    for (b, h) in dks:
+        np.testing.assert_allclose(dks[(b, h)], gk[b, cols, h], atol=1e-11)
+        np.testing.assert_allclose(dvs[(b, h)], gv[b, cols, h], atol=1e-11)
+    # and the full oracle backward agrees on those columns
+    out, lse = oa.forward(q, k, v, lens, zigzag, causal)
+    _, dk, dv = oa.backward(q, k, v, out, lse, do, lens, zigzag, causal)
+    np.testing.assert_allclose(dks[(1, 1)], dk[1, cols, 1], atol=1e-11)
+    np.testing.assert_allclose(dvs[(1, 1)], dv[1, cols, 1], atol=1e-11)
+
+
+def test_backward_cols_catch_a_planted_delta_mistake():
+    """A Delta taken with the wrong sign (planted here, on the CPU) must fail the autograd pin."""
+    lens, S, d = [6, 2, 10, 4], 22, 8
+    q, k, v, do = (rnd((1, S, 1, d), s) for s in (90, 91, 92, 93))
+    _, _, (_, gk, _) = _natural_autograd(q, k, v, do, lens, True, True)
+    _, lses, deltas = oa.row_stats(q, k, v, do, lens, True, True)
+    bad = {key: -val for key, val in deltas.items()}
+    cols = np.arange(S)
+    dks, _ = oa.backward_cols(q, k, v, do, lens, True, True, cols, lses, bad)
+    assert not np.allclose(dks[(0, 0)], gk[0, cols, 0], atol=1e-6)
