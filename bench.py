@@ -377,11 +377,13 @@ def norm_gbs(st, world, steps=10, warmup=3):
             "achieved_gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm, "peak_kind": kind + " HBM copy", "launches": 3}
 
 
-def train_step_tflops(st, world, steps=3, warmup=2):
-    """Forward + backward on the training workload (B=2, H=32, d=128, S=32768,
-    causal zigzag over Dirichlet sharding shapes): one step = st_attn_fwd (fp32
-    out) + st_attn_bwd (fp32 gradients), inputs resident in HBM."""
-    wl = WORKLOADS["train_s32768"]
+def train_step_tflops(st, world, steps=3, warmup=2, name="train_s32768"):
+    """Forward + backward on a causal zigzag workload: the training workload
+    (B=2, H=32, d=128, S=32768 over Dirichlet sharding shapes) or the 7B-style
+    one (B=1, H=32, d=128, S=131072, 8 equal shards = 16 zigzag chunks).  One
+    step = st_attn_fwd (fp32 out) + st_attn_bwd (fp32 gradients), inputs
+    resident in HBM."""
+    wl = WORKLOADS[name]
     dev = torch.device("cuda", torch.cuda.current_device())
     q, k, v, do = make_inputs(wl, seed=7, device=dev, with_dout=True)
     lay = st.Layout(wl.lens, wl.zigzag)
@@ -417,7 +419,7 @@ def train_step_tflops(st, world, steps=3, warmup=2):
         tb += ev[1].elapsed_time(ev[2])
     tf = max_over_ranks(tf / steps, world)
     tb = max_over_ranks(tb / steps, world)
-    return {"workload": "train_s32768", "shard_lens": list(wl.lens), "causal": True, "zigzag": True,
+    return {"workload": name, "shard_lens": list(wl.lens), "causal": True, "zigzag": True,
             "fwd_tflops": wl.fwd_flops() * world / (tf * 1e-3) / 1e12,
             "bwd_tflops": wl.bwd_flops() * world / (tb * 1e-3) / 1e12,
             "fwd_bwd_tflops": (wl.fwd_flops() + wl.bwd_flops()) * world / ((tf + tb) * 1e-3) / 1e12,
@@ -582,6 +584,10 @@ def run_ours(args, rank, world):
     if not args.no_train:
         cool_down()
     train = None if args.no_train else train_step_tflops(st, world)
+    llm7b = None
+    if not args.no_train and not args.bwd:
+        cool_down()
+        llm7b = train_step_tflops(st, world, name="llm7b_causal_s131072")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -611,7 +617,7 @@ def run_ours(args, rank, world):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
-            "secondary": {"train": train, "merge": merge, "mufu": mufu, "proj": proj, "mlp": mlp, "conv": conv, "norm": gnorm},
+            "secondary": {"train": train, "llm7b": llm7b, "merge": merge, "mufu": mufu, "proj": proj, "mlp": mlp, "conv": conv, "norm": gnorm},
         }
         print(json.dumps(line), flush=True)
 

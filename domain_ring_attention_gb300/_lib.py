@@ -60,6 +60,7 @@ PROTOTYPES = [
     ("st_error_string", ctypes.c_char_p, [_I]),
     ("st_last_cuda_error", _I, []),
     ("st_device_error", _I, [_P]),
+    ("st_selftest_bounded_wait", _I, [ctypes.c_longlong, _P]),
 ]
 
 _lib = None

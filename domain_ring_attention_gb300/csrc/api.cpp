@@ -92,8 +92,9 @@ extern "C" int st_device_error(void* stream) {
     const int b = st::bwd_tc_device_error(true);
     const int g = st::gemm_tc_device_error(true);
     const int c = st::conv_tc_device_error(true);
-    if (f < 0 || b < 0 || g < 0 || c < 0) return cuda_status((int)cudaGetLastError());
-    return (f || b || g || c) ? ST_ERR_DEVICE_TIMEOUT : ST_OK;
+    const int t = st::selftest_device_error(true);
+    if (f < 0 || b < 0 || g < 0 || c < 0 || t < 0) return cuda_status((int)cudaGetLastError());
+    return (f || b || g || c || t) ? ST_ERR_DEVICE_TIMEOUT : ST_OK;
 }
 
 extern "C" int st_proj_gemm(int M, int N, int K, const void* x, const void* w, void* y, int out_dtype,
@@ -344,6 +345,8 @@ extern "C" int st_attn_fwd_host(const st_layout_t* L, int B, int H, int d, int d
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
+    // ev[0]: work queued on `stream` before this call, then V landed, then the
+    // last copy back; ev[1 .. nchunks]: Q chunk c landed; the rest: chunk c computed
     std::vector<cudaEvent_t> ev(1 + 2 * nchunks, nullptr);
     for (auto& e : ev)
         if ((rc = cuda_status((int)cudaEventCreateWithFlags(&e, cudaEventDisableTiming))) != ST_OK) break;
@@ -356,6 +359,11 @@ extern "C" int st_attn_fwd_host(const st_layout_t* L, int B, int H, int d, int d
     const size_t row_bytes = (size_t)H * d * 2;            // one token of q, k, v or out (bf16)
     const size_t kv_bytes = (size_t)B * S * row_bytes;
     auto ck = [&](cudaError_t e) { return cuda_status((int)e); };
+    // The copies into q, k, v (and out of out, lse) must come after everything
+    // already queued on `stream`, which may still read or write those buffers
+    // (or memory that a stream-ordered allocator has just handed them).
+    if ((rc = ck(cudaEventRecord(ev[0], cs))) != ST_OK) return finish(rc);
+    if ((rc = ck(cudaStreamWaitEvent(xs, ev[0], 0))) != ST_OK) return finish(rc);
     // V, then K: every query tile needs all of both; the fp16 copy of V runs
     // while K is still coming in
     if ((rc = ck(cudaMemcpyAsync(v, v_host, kv_bytes, cudaMemcpyHostToDevice, xs))) != ST_OK) return finish(rc);

@@ -111,6 +111,7 @@ int fwd_tc_device_error(bool clear);
 int bwd_tc_device_error(bool clear);
 int gemm_tc_device_error(bool clear);
 int conv_tc_device_error(bool clear);
+int selftest_device_error(bool clear);
 // C[M, N] = A[M, K] W[N, K]^T on the tensor cores (bf16 in, fp32 accumulation)
 int launch_gemm_tc(int M, int N, int K, const void* a, const void* w, void* c, int out_dtype, void* stream);
 // halo exchange and sharded 2-D convolution (conv_tc.cu)

@@ -11,8 +11,6 @@
 // For them the scratch lives in a file-scope device array that is part of
 // the loaded module: every GPU that loads the library holds it (32 MiB) until
 // the process exits, and nothing is allocated per call.
-#include <mutex>
-
 #include <cuda_runtime.h>
 
 #include "common.h"
@@ -25,25 +23,15 @@ constexpr size_t kScratchBytes = size_t(32) << 20;   // 32 MiB per device
 // device symbol: its device address comes from cudaGetSymbolAddress.
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once
-// per device (on the first call made with that device current).
+// Device address of the scratch array in the current device's context.  It is
+// looked up on every call (a host-side query that allocates nothing): a
+// cached address could outlive the context it belongs to (after
+// cudaDeviceReset, or in another context on the same device).
 int scratch_on_current_device(void** ptr) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return (int)e;
-    if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return (int)e;
-        g_scratch_ptr[dev] = p;
-    }
-    *ptr = g_scratch_ptr[dev];
+    *ptr = p;
     return 0;
 }
 

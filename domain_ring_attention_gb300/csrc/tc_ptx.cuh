@@ -57,21 +57,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase with the given parity to complete.  `abort` is
 // the CTA's shared abort word: once any thread gave up, the others stop
-// waiting too.  Returns false on timeout or abort.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// waiting too.  Returns false on timeout (after `limit` clock cycles of
+// polling, recorded in the abort word and the device error word) or abort.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0) {
             if (*abort || *(volatile int*)&g_device_error) return false;
-            if (clock64() - t0 > kWaitLimitCycles) {
+            if (clock64() - t0 > limit) {
                 *abort = 1;
                 atomicExch(&g_device_error, 1);
                 return false;
             }
         }
     }
+}
+
+// The same with the kernels' default limit (~2 s).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+    return mbar_wait_limit(bar, parity, abort, kWaitLimitCycles);
 }
 
 // Bounded wait used at kernel exit for this thread's own asynchronous work

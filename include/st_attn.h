@@ -134,7 +134,8 @@ int st_attn_fwd(const st_layout_t* layout, int B, int H, int d, int dtype, int c
  *   workspace, ws_bytes    : as st_attn_fwd (pass 0).
  *   copy_stream            : a second stream, distinct from `stream`, that
  *                            carries the copies.
- * Order of work:
+ * Order of work (stream-ordered: nothing starts before the work already
+ * queued on `stream` at the call, which copy_stream is made to wait for):
  *   1. V, then K, are copied in on copy_stream; every query tile needs all of
  *      them.  The fp16 copy of V runs on `stream` while K arrives.
  *   2. Q follows on copy_stream in three chunks of query tiles: a short first
@@ -165,9 +166,10 @@ int st_attn_fwd_host(const st_layout_t* layout, int B, int H, int d, int dtype, 
  *   - problems whose workspace (st_attn_workspace_size, pass 0) exceeds
  *     32 MiB are refused with ST_ERR_SCRATCH_LIMIT before anything runs
  *     (bf16: B * S * H * d must stay below about 16.7 million);
- *   - the first call on a device, made with that device current, looks up
- *     the array's device address; make that first call before any stream
- *     capture;
+ *   - every call looks up the array's device address in the current
+ *     device's context (a host-side query that allocates nothing); the first
+ *     call on a device may also load the library's device code there, so
+ *     make that first call before any stream capture;
  *   - every call on a device uses the same array, so calls whose GPU work
  *     overlaps (on different streams, or from different host threads) race
  *     and must be ordered by the caller.  The array keeps the last call's
@@ -389,6 +391,17 @@ int st_group_norm_sharded(int D, const int64_t* rows, int W, int C, int G, float
  * barrier waits gave up since the last call (the kernel then stopped early
  * and its outputs are not valid), else ST_OK.  Blocks the host. */
 int st_device_error(void* stream);
+
+/* Self-test of the bounded device waits (failure detection; the paper has no
+ * counterpart).  Launches one CTA of one warp on `stream` that initialises an
+ * mbarrier nothing ever arrives at and waits on it with the kernels' bounded
+ * wait, giving up after limit_cycles clock cycles of polling (1 .. 4e9; the
+ * kernels' own limit is 4e9, about 2 s).  No copy, MMA or tensor-memory
+ * allocation is in flight, so the kernel only records the timeout in the
+ * device error word and returns: st_device_error then reports
+ * ST_ERR_DEVICE_TIMEOUT once and clears it, and the context stays usable.
+ * Errors: ST_ERR_INVALID_ARG (limit out of range), ST_ERR_CUDA (launch). */
+int st_selftest_bounded_wait(long long limit_cycles, void* stream);
 
 /* Human-readable text for a status code (static storage). */
 const char* st_error_string(int code);

@@ -212,3 +212,10 @@ def test_bindings_refuse_host_memory(lib):
         assert e.value.code == -10, e.value
     assert lib.st_is_device_pointer(ctypes.c_void_p(x.data_ptr())) == 0
     assert lib.st_error_string(-10).decode().startswith("a pointer that must address device memory")
+
+
+def test_bounded_wait_selftest_rejects_bad_limits(lib):
+    """The wait limit is checked on the host before anything is launched."""
+    assert lib.st_selftest_bounded_wait(0, None) == -8
+    assert lib.st_selftest_bounded_wait(-5, None) == -8
+    assert lib.st_selftest_bounded_wait(5 * 10 ** 9, None) == -8

@@ -47,3 +47,29 @@ def test_host_forward_equals_device_forward(B, H, d, lens, causal, zigzag):
     err = np.abs(f64(out_h[0, rows, 0]) - o)
     assert err.max() <= 1e-2, err.max()
     assert np.abs(f64(lse_h[0, 0, rows]) - l).max() <= 1e-2
+
+
+def test_host_forward_waits_for_work_already_queued_on_its_stream():
+    """The copies run on a second stream, but only after the work queued on `stream` before the call: here
+    `stream` first spins (~25 ms) and then overwrites the device staging buffer of v.  A copy that started at
+    once would be overwritten by that late write; the call must instead copy v in after it, and give the outputs
+    of st_attn_fwd bit for bit."""
+    wl = Workload("order", B=1, H=4, d=64, lens=(512,) * 8, causal=False, zigzag=False, dtype="bf16")
+    q, k, v = make_inputs(wl, seed=5)
+    lay = st.Layout(wl.lens)
+    ref_out, ref_lse = st.st_attn_fwd(lay, q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    pin = [x.pin_memory() for x in (q, k, v)]
+    out_h = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
+    lse_h = torch.empty(tuple(ref_lse.shape), dtype=torch.float32, pin_memory=True)
+    dev = {"q": torch.empty_like(ref_out), "k": torch.empty_like(ref_out), "v": torch.empty_like(ref_out),
+           "out": torch.empty_like(ref_out), "lse": torch.empty_like(ref_lse)}
+    stream, copy_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(50_000_000)
+        dev["v"].fill_(7.0)
+    st.st_attn_fwd_host(lay, pin[0], pin[1], pin[2], out_h, lse_h, dev, stream=stream, copy_stream=copy_stream)
+    stream.synchronize()
+    assert_no_device_error()
+    assert torch.equal(out_h, ref_out.cpu())
+    assert torch.equal(lse_h, ref_lse.cpu())
