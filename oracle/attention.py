@@ -404,3 +404,22 @@ def backward_cols(q, k, v, dout, lens, zigzag, causal, cols, lse, delta, scale=N
         dvs[(b, h)] = p.T @ dout[b, :, h]
         dks[(b, h)] = scale * (ds.T @ q[b, :, h])
     return dks, dvs
+
+
+def block_grads(qb, kb, vb, dob, lse_b, delta_b, qpos, kpos, causal, scale):
+    """One (query shard, KV shard) block's share of the backward.
+
+    qb, dob [n, d] with their rows' full lse_b and Delta_b [n]; kb, vb [m, d].
+    Over the visible pairs of the block, with P_ij = exp(s_ij - lse_i):
+    dQ_i = scale sum_j dS_ij k_j, dK_j = scale sum_i dS_ij q_i, dV_j = sum_i
+    P_ij dO_i.  Summed over every block of a layout these are the gradients of
+    ``backward``: each pair (i, j) lies in exactly one block.
+    """
+    qb, kb, vb, dob = _as_f64(qb), _as_f64(kb), _as_f64(vb), _as_f64(dob)
+    lse_b, delta_b = _as_f64(lse_b), _as_f64(delta_b)
+    s = scale * (qb @ kb.T)
+    vis = _visible(np.asarray(qpos), np.asarray(kpos), causal)
+    p = np.exp(np.where(vis, s - lse_b[:, None], NEG_INF))
+    dp = dob @ vb.T
+    ds = p * (dp - delta_b[:, None])
+    return scale * (ds @ kb), scale * (ds.T @ qb), p.T @ dob

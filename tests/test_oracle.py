@@ -425,3 +425,32 @@ def test_backward_cols_catch_a_planted_delta_mistake():
     cols = np.arange(S)
     dks, _ = oa.backward_cols(q, k, v, do, lens, True, True, cols, lses, bad)
     assert not np.allclose(dks[(0, 0)], gk[0, cols, 0], atol=1e-6)
+
+
+@pytest.mark.parametrize("lens,zigzag,causal", [([6, 2, 10, 4], True, True), ([5, 9, 3], False, False),
+                                                ([4, 4], False, True)])
+def test_block_grads_sum_to_the_backward(lens, zigzag, causal):
+    """Every (query shard, KV shard) block's share, summed over the blocks, gives the full backward
+    (itself pinned by autograd and finite differences)."""
+    S, d = sum(lens), 8
+    q, k, v, do = (rnd((1, S, 2, d), s) for s in (100, 101, 102, 103))
+    out, lse = oa.forward(q, k, v, lens, zigzag, causal)
+    gq, gk, gv = oa.backward(q, k, v, out, lse, do, lens, zigzag, causal)
+    pos = ol.natural_positions(lens, zigzag)
+    off = ol.shard_offsets(lens)
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for h in range(2):
+        delta = np.sum(do[0, :, h] * out[0, :, h], axis=1)
+        for r in range(len(lens)):
+            qs = slice(off[r], off[r + 1])
+            for j in range(len(lens)):
+                ks = slice(off[j], off[j + 1])
+                a, b, c = oa.block_grads(q[0, qs, h], k[0, ks, h], v[0, ks, h], do[0, qs, h], lse[0, h, qs],
+                                         delta[qs], pos[qs], pos[ks], causal, scale)
+                dq[0, qs, h] += a
+                dk[0, ks, h] += b
+                dv[0, ks, h] += c
+    np.testing.assert_allclose(dq, gq, atol=1e-12)
+    np.testing.assert_allclose(dk, gk, atol=1e-12)
+    np.testing.assert_allclose(dv, gv, atol=1e-12)
