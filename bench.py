@@ -238,6 +238,58 @@ def merge_gbs(st, wl, world, steps=10, warmup=3):
             "achieved_gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm, "peak_kind": kind + " HBM copy"}
 
 
+def hbm_steps_gbs(st, world, steps=10, warmup=3):
+    """The backward's bandwidth-bound steps on their own, at the training
+    workload's shapes (B=2, S=32768, H=32, d=128): Delta = rowsum(dO o O)
+    (st_attn_bwd_delta: fp32 out and bf16 dO read, 4 B per row written), the
+    fp32 -> bf16 conversion of the dQ accumulator (st_convert_f32: 4 B read,
+    2 B written per element) and the exact fp16 operand copy of one bf16
+    tensor (st_fp16_scaled_copy: its max pass and its copy pass read the
+    tensor twice and write the copy once, 6 B per element).  Each is
+    reported as its bytes / CUDA-event time against the measured HBM copy;
+    the tensors (0.5-1 GiB each) exceed L2."""
+    from domain_ring_attention_gb300 import _lib
+    wl = WORKLOADS["train_s32768"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(29)
+    shape = (wl.B, wl.S, wl.H, wl.d)
+    n = wl.B * wl.S * wl.H * wl.d
+    out32 = torch.randn(shape, device=dev, generator=g)
+    do16 = torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+    delta = torch.empty((wl.B, wl.H, wl.S), device=dev)
+    dst16 = torch.empty(shape, device=dev, dtype=torch.bfloat16)
+    h16 = torch.empty(shape, device=dev, dtype=torch.float16)
+    exps = torch.zeros(4, device=dev, dtype=torch.int32)
+    scratch = torch.zeros(4, device=dev, dtype=torch.int32)
+    stream = torch.cuda.current_stream()
+    jobs = {
+        "delta": (lambda: _lib.st_attn_bwd_delta(out32, do16, delta=delta, stream=stream),
+                  n * 4 + n * 2 + wl.B * wl.H * wl.S * 4, "delta_kernel (st_attn_bwd_delta)", 1),
+        "convert": (lambda: _lib.st_convert_f32(out32, torch.bfloat16, out=dst16, stream=stream),
+                    n * 4 + n * 2, "convert_kernel (st_convert_f32)", 1),
+        "fp16_copy": (lambda: _lib.st_fp16_scaled_copy(do16, out=h16, exps=exps, scratch=scratch, stream=stream),
+                      n * 2 * 2 + n * 2, "amax_kernel + fp16_copy_kernel (st_fp16_scaled_copy)", 2),
+    }
+    _, _, hbm, kind = peaks()
+    res = {}
+    for name, (fn, nbytes, kernel, launches) in jobs.items():
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"kernel": kernel, "bytes_per_call": nbytes, "ms": ms, "achieved_gbs": gbs, "peak_gbs": hbm,
+                     "frac": gbs / hbm, "peak_kind": kind + " HBM copy", "launches": launches}
+    return res
+
+
 def proj_tflops(st, wl, world, steps=10, warmup=3):
     """The projections on either side of the attention for the workload's
     shape (st_proj_gemm, bf16 in, fp32 accumulation, bf16 out): the packed
@@ -567,10 +619,12 @@ def run_ours(args, rank, world):
     # the secondary kernels after the end-to-end run, each after a pause so
     # that none starts under the power cap that the previous one ran into;
     # the gated MLP, which draws the most, goes last
-    merge = proj = mlp = conv = gnorm = None
+    merge = proj = mlp = conv = gnorm = hbm_steps = None
     if not args.no_train and world == 1 and not args.bwd:
         cool_down()
         merge = merge_gbs(st, wl, world)
+        cool_down()
+        hbm_steps = hbm_steps_gbs(st, world)
         cool_down()
         proj = proj_tflops(st, wl, world)
         cool_down()
@@ -617,7 +671,7 @@ def run_ours(args, rank, world):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
-            "secondary": {"train": train, "llm7b": llm7b, "merge": merge, "mufu": mufu, "proj": proj, "mlp": mlp, "conv": conv, "norm": gnorm},
+            "secondary": {"train": train, "llm7b": llm7b, "merge": merge, "bwd_hbm_steps": hbm_steps, "mufu": mufu, "proj": proj, "mlp": mlp, "conv": conv, "norm": gnorm},
         }
         print(json.dumps(line), flush=True)
 

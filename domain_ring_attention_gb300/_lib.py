@@ -43,7 +43,7 @@ PROTOTYPES = [
     ("st_attn_fwd_host", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                               _P, _P]),
     ("st_attn_fwd_noalloc", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P]),
-    ("st_attn_fwd_partials", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P]),
+    ("st_attn_fwd_partials", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     ("st_attn_merge", _I, [_I, _I, _I, _I64, _I, _P, _P, _P, _P, _I, _P]),
     ("st_attn_bwd", _I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P, _P, _I, _P, _P, _P,
                          _P, _SZ, _P]),
@@ -61,6 +61,18 @@ PROTOTYPES = [
     ("st_last_cuda_error", _I, []),
     ("st_device_error", _I, [_P]),
     ("st_selftest_bounded_wait", _I, [ctypes.c_longlong, _P]),
+    ("st_ring_workspace_size", _I, [_P, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
+    ("st_attn_bwd_delta", _I, [_I, _I, _I64, _I, _I, _P, _I, _P, _P, _P]),
+    ("st_convert_f32", _I, [_I64, _P, _P, _I, _P]),
+    ("st_fp16_scaled_copy", _I, [_I64, _P, _P, _P, _P, _P]),
+    ("st_ring_fwd_step", _I, [_P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _P, _P, _P, _SZ, _P]),
+    ("st_ring_bwd_step", _I, [_P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _I, _P, _P, _I, _P, _P, _P,
+                              _P, _SZ, _P]),
+    ("st_ring_fwd_local", _I, [_P, _I, _I, _I, _I, _F, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P),
+                               _I, ctypes.POINTER(_P), ctypes.POINTER(_P), _P, _SZ, _P, _P]),
+    ("st_ring_bwd_local", _I, [_P, _I, _I, _I, _I, _F, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P),
+                               ctypes.POINTER(_P), _I, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P),
+                               ctypes.POINTER(_P), ctypes.POINTER(_P), _P, _SZ, _P, _P]),
 ]
 
 _lib = None
@@ -246,15 +258,20 @@ def st_attn_fwd_host(layout, q_host, k_host, v_host, out_host, lse_host, dev, ca
     return out_host, lse_host
 
 
-def st_attn_fwd_partials(layout, q, k, v, causal=False, scale=0.0, stream=None):
-    """Per-KV-shard partials: (partial_out [D,B,S,H,d] fp32, partial_lse [D,B,H,S])."""
+def st_attn_fwd_partials(layout, q, k, v, causal=False, scale=0.0, stream=None, workspace=None):
+    """Per-KV-shard partials: (partial_out [D,B,S,H,d] fp32, partial_lse [D,B,H,S]).
+    ``workspace`` as st_attn_fwd (allocated here when not given)."""
     B, S, H, d = _shape(q)
     D = layout.D
     po = torch.empty((D, B, S, H, d), device=q.device, dtype=torch.float32)
     pl = torch.empty((D, B, H, S), device=q.device, dtype=torch.float32)
+    if workspace is None:
+        need = st_attn_workspace_size(layout, B, H, d, q.dtype, 0)
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
     _check(load().st_attn_fwd_partials(layout.handle, B, H, d, _dtype_code(q.dtype),
                                        int(bool(causal)), float(scale), _ptr(q), _ptr(k), _ptr(v),
-                                       _ptr(po), _ptr(pl), _stream(stream)), "st_attn_fwd_partials")
+                                       _ptr(po), _ptr(pl), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)), "st_attn_fwd_partials")
     return po, pl
 
 
@@ -439,3 +456,128 @@ def st_group_norm_sharded(shards, G, gamma=None, beta=None, eps=1e-5, out_dtype=
                                      _dtype_code(out[0].dtype), _ptr(workspace), workspace.numel(),
                                      _stream(stream)), "st_group_norm_sharded")
     return out
+
+
+# ---------------------------------------------------------------- ring attention across ranks
+
+def st_ring_workspace_size(layout, B, H, d, which):
+    n = _SZ()
+    _check(load().st_ring_workspace_size(layout.handle, B, H, d, which, ctypes.byref(n)),
+           "st_ring_workspace_size")
+    return int(n.value)
+
+
+def st_ring_fwd_step(layout, q_shard, kv_shard, q, k, v, prev=None, causal=False, scale=0.0,
+                     out_dtype=torch.float32, out=None, lse=None, workspace=None, stream=None):
+    """One ring step of rank ``q_shard``: q [B, L_q, H, d] against the K/V block
+    [B, L_kv, H, d] of shard ``kv_shard`` (bf16), merged into ``prev`` (a pair
+    (out fp32, lse) of the running state, or None at the first step).
+    Returns (out, lse); out may be ``prev[0]`` itself (fp32)."""
+    B, Lq, H, d = _shape(q)
+    Lkv = int(k.shape[1])
+    _check_tensor(q, (B, Lq, H, d), torch.bfloat16, "q")
+    _check_tensor(k, (B, Lkv, H, d), torch.bfloat16, "k")
+    _check_tensor(v, (B, Lkv, H, d), torch.bfloat16, "v")
+    if out is None:
+        out = torch.empty((B, Lq, H, d), device=q.device, dtype=out_dtype)
+    if lse is None:
+        lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32)
+    if workspace is None:
+        workspace = torch.empty(st_ring_workspace_size(layout, B, H, d, 0), device=q.device, dtype=torch.uint8)
+    po, pl = (None, None) if prev is None else prev
+    _check(load().st_ring_fwd_step(layout.handle, int(q_shard), int(kv_shard), B, H, d, ST_DTYPE_BF16,
+                                   int(bool(causal)), float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(po), _ptr(pl),
+                                   _dtype_code(out.dtype), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                   _stream(stream)), "st_ring_fwd_step")
+    return out, lse
+
+
+def st_ring_bwd_step(layout, q_shard, kv_shard, q, k, v, out, lse, dout, dq, dk, dv, first_q, causal=False,
+                     scale=0.0, workspace=None, stream=None):
+    """One backward ring step: adds the block's contributions to the fp32
+    ``dq`` (zeroed first when ``first_q``), ``dk`` and ``dv``."""
+    B, Lq, H, d = _shape(q)
+    if workspace is None:
+        workspace = torch.empty(st_ring_workspace_size(layout, B, H, d, 1), device=q.device, dtype=torch.uint8)
+    _check(load().st_ring_bwd_step(layout.handle, int(q_shard), int(kv_shard), B, H, d, ST_DTYPE_BF16,
+                                   int(bool(causal)), float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                   _dtype_code(out.dtype), _ptr(lse), _ptr(dout), int(bool(first_q)), _ptr(dq),
+                                   _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "st_ring_bwd_step")
+    return dq, dk, dv
+
+
+def _ptrs(ts):
+    return (_P * len(ts))(*[t.data_ptr() for t in ts])
+
+
+def st_ring_fwd_local(layout, qs, ks, vs, causal=False, scale=0.0, out_dtype=torch.bfloat16, stream=None,
+                      copy_stream=None, workspace=None):
+    """The ring forward with the D ranks on this GPU: lists of per-rank shards
+    qs, ks, vs ([B, L_r, H, d] bf16).  Returns (outs, lses), per rank."""
+    D = layout.D
+    B, _, H, d = _shape(qs[0])
+    dev = qs[0].device
+    outs = [torch.empty((B, L, H, d), device=dev, dtype=out_dtype) for L in layout.lens]
+    lses = [torch.empty((B, H, L), device=dev, dtype=torch.float32) for L in layout.lens]
+    if workspace is None:
+        workspace = torch.empty(st_ring_workspace_size(layout, B, H, d, 2), device=dev, dtype=torch.uint8)
+    if copy_stream is None:
+        copy_stream = torch.cuda.Stream(device=dev)
+    _check(load().st_ring_fwd_local(layout.handle, B, H, d, int(bool(causal)), float(scale), _ptrs(qs), _ptrs(ks),
+                                    _ptrs(vs), _dtype_code(out_dtype), _ptrs(outs), _ptrs(lses), _ptr(workspace),
+                                    workspace.numel(), _stream(stream), _stream(copy_stream)), "st_ring_fwd_local")
+    return outs, lses
+
+
+def st_ring_bwd_local(layout, qs, ks, vs, outs, lses, douts, causal=False, scale=0.0, stream=None,
+                      copy_stream=None, workspace=None):
+    """The ring backward with the D ranks on this GPU.  Returns per-rank fp32
+    (dqs, dks, dvs)."""
+    B, _, H, d = _shape(qs[0])
+    dev = qs[0].device
+    mk = lambda: [torch.empty((B, L, H, d), device=dev, dtype=torch.float32) for L in layout.lens]
+    dqs, dks, dvs = mk(), mk(), mk()
+    if workspace is None:
+        workspace = torch.empty(st_ring_workspace_size(layout, B, H, d, 3), device=dev, dtype=torch.uint8)
+    if copy_stream is None:
+        copy_stream = torch.cuda.Stream(device=dev)
+    _check(load().st_ring_bwd_local(layout.handle, B, H, d, int(bool(causal)), float(scale), _ptrs(qs), _ptrs(ks),
+                                    _ptrs(vs), _ptrs(outs), _dtype_code(outs[0].dtype), _ptrs(lses), _ptrs(douts),
+                                    _ptrs(dqs), _ptrs(dks), _ptrs(dvs), _ptr(workspace), workspace.numel(),
+                                    _stream(stream), _stream(copy_stream)), "st_ring_bwd_local")
+    return dqs, dks, dvs
+
+
+# ---------------------------------------------------------------- the backward's HBM-bound steps on their own
+
+def st_attn_bwd_delta(out, dout, delta=None, stream=None):
+    """Delta [B, H, S] fp32 = rowsum(dout * out) of BSHD tensors (out bf16 or fp32, dout bf16 or fp32)."""
+    B, S, H, d = _shape(dout)
+    if delta is None:
+        delta = torch.empty((B, H, S), device=dout.device, dtype=torch.float32)
+    _check(load().st_attn_bwd_delta(B, H, S, d, _dtype_code(dout.dtype), _ptr(out), _dtype_code(out.dtype),
+                                    _ptr(dout), _ptr(delta), _stream(stream)), "st_attn_bwd_delta")
+    return delta
+
+
+def st_convert_f32(src, dtype=torch.bfloat16, out=None, stream=None):
+    """fp32 tensor -> ``dtype`` (bf16 rounded to nearest even, or an fp32 copy)."""
+    if out is None:
+        out = torch.empty(src.shape, device=src.device, dtype=dtype)
+    _check(load().st_convert_f32(src.numel(), _ptr(src), _ptr(out), _dtype_code(out.dtype), _stream(stream)),
+           "st_convert_f32")
+    return out
+
+
+def st_fp16_scaled_copy(src, out=None, exps=None, scratch=None, stream=None):
+    """Exact fp16 copy of a bf16 tensor scaled by 2^-e: returns (copy, e as a device int32 tensor)."""
+    if out is None:
+        out = torch.empty(src.shape, device=src.device, dtype=torch.float16)
+    if exps is None:
+        exps = torch.zeros(4, device=src.device, dtype=torch.int32)
+    if scratch is None:
+        scratch = torch.zeros(4, device=src.device, dtype=torch.int32)
+    _check(load().st_fp16_scaled_copy(src.numel(), _ptr(src), _ptr(out), _ptr(exps), _ptr(scratch),
+                                      _stream(stream)), "st_fp16_scaled_copy")
+    return out, exps

@@ -420,7 +420,7 @@ extern "C" int st_attn_fwd_host(const st_layout_t* L, int B, int H, int d, int d
 extern "C" int st_attn_fwd_partials(const st_layout_t* L, int B, int H, int d, int dtype,
                                     int causal, float scale, const void* q, const void* k,
                                     const void* v, float* partial_out, float* partial_lse,
-                                    void* stream) {
+                                    void* workspace, size_t ws_bytes, void* stream) {
     int rc = check_common(L, B, H, d, dtype, &scale);
     if (rc != ST_OK) return rc;
     if (!q || !k || !v || !partial_out || !partial_lse) return ST_ERR_NULL;
@@ -428,7 +428,25 @@ extern "C" int st_attn_fwd_partials(const st_layout_t* L, int B, int H, int d, i
         !aligned16(partial_lse))
         return ST_ERR_MISALIGNED;
     st::AttnArgs a{q, k, v, nullptr, nullptr, partial_out, partial_lse, B, H, d, causal ? 1 : 0, scale,
-                   ST_DTYPE_F32};
+                   ST_DTYPE_F32, nullptr, nullptr, nullptr};
+    if (dtype == ST_DTYPE_BF16) {
+        const int64_t rows = (int64_t)B * L->S * H;
+        const size_t need = st::fwd_workspace_bytes(rows, d, dtype);
+        if (!workspace || ws_bytes < need) return ST_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return ST_ERR_MISALIGNED;
+        if (!all_on_device(q, k, v, partial_out, partial_lse, workspace)) return ST_ERR_NOT_DEVICE;
+        // the tensor-core forward with its state written out (and restarted) per KV shard
+        char* ws = static_cast<char*>(workspace);
+        a.v16 = ws;
+        a.amax_bits = reinterpret_cast<unsigned*>(ws + need - 256);
+        a.exps = reinterpret_cast<int*>(ws + need - 128);
+        rc = cuda_status(st::launch_fp16_copy1(v, a.v16, rows * d, a.amax_bits, a.exps, stream));
+        if (rc != ST_OK) return rc;
+        bool handled = false;
+        rc = st::launch_fwd_tc(*L, a, stream, &handled);
+        if (handled) return cuda_status(rc);
+        return ST_ERR_UNSUPPORTED;
+    }
     if (!all_on_device(q, k, v, partial_out, partial_lse)) return ST_ERR_NOT_DEVICE;
     st::SegTable t;
     st::fill_segtable(*L, 64, &t);
@@ -534,4 +552,47 @@ extern "C" int st_permute(const st_layout_t* L, int B, int H, int d, int dtype, 
     st::SegTable t;
     st::fill_segtable(*L, 64, &t);
     return cuda_status(st::launch_permute(t, B, H, d, dtype, to_natural ? 1 : 0, in, out, stream));
+}
+
+extern "C" int st_attn_bwd_delta(int B, int H, int64_t S, int d, int dtype, const void* out, int out_dtype,
+                                 const void* dout, float* delta, void* stream) {
+    if (!out || !dout || !delta) return ST_ERR_NULL;
+    if (B < 1 || H < 1 || S < 1 || S >= INT32_MAX) return ST_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ST_ERR_UNSUPPORTED;
+    if (dtype != ST_DTYPE_F32 && dtype != ST_DTYPE_BF16) return ST_ERR_UNSUPPORTED;
+    if (out_dtype != ST_DTYPE_F32 && out_dtype != dtype) return ST_ERR_UNSUPPORTED;
+    if (!aligned16(out) || !aligned16(dout) || !aligned16(delta)) return ST_ERR_MISALIGNED;
+    if (!all_on_device(out, dout, delta)) return ST_ERR_NOT_DEVICE;
+    st::BwdArgs a{};
+    a.out = out;
+    a.dout = dout;
+    a.delta = delta;
+    a.B = B;
+    a.H = H;
+    a.d = d;
+    a.out_dtype = out_dtype;
+    return cuda_status(st::launch_bwd_preprocess(a, S, dtype, stream));
+}
+
+extern "C" int st_convert_f32(int64_t n, const float* src, void* dst, int dst_dtype, void* stream) {
+    if (!src || !dst) return ST_ERR_NULL;
+    if (n < 1) return ST_ERR_INVALID_ARG;
+    if (dst_dtype != ST_DTYPE_F32 && dst_dtype != ST_DTYPE_BF16) return ST_ERR_UNSUPPORTED;
+    if (!aligned16(src) || !aligned16(dst)) return ST_ERR_MISALIGNED;
+    if (!all_on_device(src, dst)) return ST_ERR_NOT_DEVICE;
+    st::BwdArgs a{};
+    a.dq_acc = const_cast<float*>(src);
+    a.dq = dst;
+    a.B = 1;
+    a.H = 1;
+    a.d = 1;
+    return cuda_status(st::launch_dq_convert(a, n, dst_dtype, stream));
+}
+
+extern "C" int st_fp16_scaled_copy(int64_t n, const void* src, void* dst, int* exps, void* scratch, void* stream) {
+    if (!src || !dst || !exps || !scratch) return ST_ERR_NULL;
+    if (n < 8 || n % 8 != 0) return ST_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst) || !aligned16(exps) || !aligned16(scratch)) return ST_ERR_MISALIGNED;
+    if (!all_on_device(src, dst, exps, scratch)) return ST_ERR_NOT_DEVICE;
+    return cuda_status(st::launch_fp16_copy1(src, dst, n, static_cast<unsigned*>(scratch), exps, stream));
 }

@@ -235,9 +235,10 @@ __device__ __forceinline__ int norm_exp(float amax, int target) {
 struct Fp16Job {
     const uint4* src[4];
     uint4* dst[4];
+    int64_t n8[4];     // 8-element units of each tensor (n8 of the launch = the largest)
 };
 
-// max |x| of NT bf16 tensors of n8 * 8 elements each (float bits, atomicMax)
+// max |x| of NT bf16 tensors of job.n8[t] * 8 elements each (float bits, atomicMax)
 template <int NT>
 __global__ void __launch_bounds__(256)
 amax_kernel(int64_t n8, const __grid_constant__ Fp16Job job, unsigned* __restrict__ amax_bits) {
@@ -247,6 +248,7 @@ amax_kernel(int64_t n8, const __grid_constant__ Fp16Job job, unsigned* __restric
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
+            if (i >= job.n8[t]) continue;
             const uint4 x = job.src[t][i];
             const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -287,6 +289,7 @@ fp16_copy_kernel(int64_t n8, int ds_d, const __grid_constant__ Fp16Job job,
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
+            if (i >= job.n8[t]) continue;
             const uint4 x = job.src[t][i];
             const uint32_t w[4] = {x.x, x.y, x.z, x.w};
             uint32_t r[4];
@@ -315,13 +318,16 @@ int fp16_grid(int64_t n8) {
 
 }  // namespace
 
-int launch_fp16_copies(const BwdArgs& a, int64_t S, void* stream) {
-    const int64_t n8 = (int64_t)a.B * S * a.H * a.d / 8;
+int launch_fp16_copies(const BwdArgs& a, int64_t S, void* stream, int64_t Skv) {
+    if (Skv < 0) Skv = S;
+    const int64_t nq8 = (int64_t)a.B * S * a.H * a.d / 8, nkv8 = (int64_t)a.B * Skv * a.H * a.d / 8;
+    const int64_t n8 = nq8 > nkv8 ? nq8 : nkv8;
     Fp16Job job;
     const void* src[4] = {a.q, a.k, a.v, a.dout};
     for (int t = 0; t < 4; ++t) {
         job.src[t] = static_cast<const uint4*>(src[t]);
         job.dst[t] = static_cast<uint4*>(a.h16[t]);
+        job.n8[t] = (t == 1 || t == 2) ? nkv8 : nq8;   // q, dO: the query rows; k, v: the key rows
     }
     const int grid = fp16_grid(n8);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -336,6 +342,7 @@ int launch_fp16_copy1(const void* src, void* dst, int64_t elems, unsigned* amax_
     Fp16Job job{};
     job.src[0] = static_cast<const uint4*>(src);
     job.dst[0] = static_cast<uint4*>(dst);
+    job.n8[0] = n8;
     const int grid = fp16_grid(n8);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(amax_bits, 0, sizeof(unsigned), st);

@@ -86,7 +86,9 @@ struct BwdParams {
     CUtensorMap tv;
     CUtensorMap tdo;
     CUtensorMap tdq;          // dq_acc, fp32, box 32 x 32 rows, 128-byte swizzle
-    SegTable tab;             // 128-row tiles
+    SegTable tab;             // 128-row key tiles (k, v, dk, dv)
+    SegTable qtab;            // 128-row query tiles (q, dO, lse, Delta, dq): the same
+                              // layout, or in a ring step another shard
     const float* lse;         // [B,H,S]
     const float* delta;       // [B,H,S]
     float* dq_acc;            // [B,S,H,D] fp32
@@ -98,6 +100,7 @@ struct BwdParams {
     float scale_log2;
     int causal;
     int grad_f32;             // dK / dV written as fp32 (else bf16)
+    int accum;                // ring step: dK / dV added into the fp32 outputs
     int use_order;            // causal: CTAs take key tiles heaviest first
     uint16_t order[kMaxOrder];
 };
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kMiscOff + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int H = p.H, S = p.tab.S;
+    const int H = p.H, S = p.tab.S, Sq = p.qtab.S;
     const int b = blockIdx.y / H, h = blockIdx.y % H;
     const int tile = p.use_order ? (int)p.order[blockIdx.x] : (int)blockIdx.x;
     const QTile kt = locate_qtile(p.tab, tile, kT);           // this CTA's key tile
@@ -217,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int64_t lse_base = ((int64_t)b * H + h) * S;
+    const int64_t lse_base = ((int64_t)b * H + h) * Sq;
 
     if (warp == 0) {
         // ------------------------------------------------ producer
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const float ds_mul = ldexpf(1.f, -p.exps[4] - kPShift);
         int i = 0;
         bool ok = true;
-        ring_walk_q(p.tab, kt.shard, [&](int q0, int nq, int natq) {
+        ring_walk_q(p.qtab, kt.shard, [&](int q0, int nq, int natq) {
             if (!ok || !active(nq, natq)) return;
             const int s = i % C::kStages;
             // fetched before the stage is free, so the global loads overlap the wait
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             bool ok = mbar_wait(bar_kv, 0, abort_flag);
             tc_fence_after();
             int i = 0;
-            ring_walk_q(p.tab, kt.shard, [&](int, int nq, int natq) {
+            ring_walk_q(p.qtab, kt.shard, [&](int, int nq, int natq) {
                 if (!ok || !active(nq, natq)) return;
                 const int s = i % C::kStages;
                 const uint64_t st = (uint64_t)(s * (C::kTileBytes >> 4));
@@ -560,13 +563,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         };
         int i = 0;
         bool ok = true;
-        ring_walk_q(p.tab, kt.shard, [&](int q0, int nq, int natq) {
+        ring_walk_q(p.qtab, kt.shard, [&](int q0, int nq, int natq) {
             if (!ok || !active(nq, natq)) return;
             if (flush_tile && i > 0 && (i % kFlush) == 0) {
                 // promote the finished segment (all MMAs of iteration i-1 done:
                 // waited for in the drain)
                 tc_fence_after();
-                emit(true, flushed);
+                emit(true, flushed || p.accum);
                 flushed = true;
             }
             const int s = i % C::kStages;
@@ -606,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // last tile's MMAs were waited for in its drain)
         if (ok) {
             tc_fence_after();
-            emit(i > 0, flushed);
+            emit(i > 0, flushed || p.accum);
         }
         // the staged dQ reductions have completed before the CTA exits
         if (lane == 0) bulk_wait_all();
@@ -671,15 +674,16 @@ bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int d) {
 }
 
 template <int D>
-int launch_t(const st_layout& L, const BwdArgs& a, void* stream) {
+int launch_t(const st_layout& Lq, const st_layout& L, const BwdArgs& a, void* stream) {
     using C = Cfg<D>;
     BwdParams p;
-    const int S = (int)L.S;
-    if (!make_map(&p.tq, a.h16[0], a.B, S, a.H, D) || !make_map(&p.tk, a.h16[1], a.B, S, a.H, D) ||
-        !make_map(&p.tv, a.h16[2], a.B, S, a.H, D) || !make_map(&p.tdo, a.h16[3], a.B, S, a.H, D) ||
-        !make_map_dq(&p.tdq, a.dq_acc, a.B, S, a.H, D))
+    const int Sq = (int)Lq.S, S = (int)L.S;
+    if (!make_map(&p.tq, a.h16[0], a.B, Sq, a.H, D) || !make_map(&p.tk, a.h16[1], a.B, S, a.H, D) ||
+        !make_map(&p.tv, a.h16[2], a.B, S, a.H, D) || !make_map(&p.tdo, a.h16[3], a.B, Sq, a.H, D) ||
+        !make_map_dq(&p.tdq, a.dq_acc, a.B, Sq, a.H, D))
         return (int)cudaErrorInvalidValue;
     fill_segtable(L, kT, &p.tab);
+    fill_segtable(Lq, kT, &p.qtab);
     // Longest-processing-time-first order for causal work: a key tile starting
     // at natural position n is seen by about S - n query rows.
     p.use_order = 0;
@@ -706,6 +710,7 @@ int launch_t(const st_layout& L, const BwdArgs& a, void* stream) {
     p.scale_log2 = a.scale * kLog2e;
     p.causal = a.causal;
     p.grad_f32 = a.grad_dtype == ST_DTYPE_F32 ? 1 : 0;
+    p.accum = a.accum && p.grad_f32 ? 1 : 0;
     auto kern = bwd_tc_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return (int)e;
@@ -716,9 +721,13 @@ int launch_t(const st_layout& L, const BwdArgs& a, void* stream) {
 
 }  // namespace
 
+int launch_bwd_tc2(const st_layout& Lq, const st_layout& Lkv, const BwdArgs& a, void* stream) {
+    return a.d == 64 ? launch_t<64>(Lq, Lkv, a, stream) : launch_t<128>(Lq, Lkv, a, stream);
+}
+
 int launch_bwd_tc(const st_layout& L, const BwdArgs& a, void* stream, bool* handled) {
     *handled = true;
-    return a.d == 64 ? launch_t<64>(L, a, stream) : launch_t<128>(L, a, stream);
+    return launch_bwd_tc2(L, L, a, stream);
 }
 
 int bwd_tc_device_error(bool clear) {

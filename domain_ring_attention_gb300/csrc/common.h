@@ -41,6 +41,9 @@ struct SegTable {
 };
 
 void fill_segtable(const st_layout& L, int tile_rows, SegTable* t);
+// The layout of shard r alone, as one rank holds it: D = 1, buffer rows
+// 0 .. L_r - 1, the shard's segments with their natural positions.
+st_layout shard_layout(const st_layout& L, int r);
 
 // Arguments common to the attention kernels.
 struct AttnArgs {
@@ -59,6 +62,10 @@ struct AttnArgs {
     void* v16;
     unsigned* amax_bits;
     int* exps;
+    // ring step: the running state (fp32 [B,Sq,H,d] and [B,H,Sq]) that this
+    // call's partial is merged into by the log-sum-exp rule, or nullptr
+    const float* prev_out;
+    const float* prev_lse;
 };
 
 // Workspace of st_attn_fwd: bf16 needs the fp16 copy of v plus 256 bytes.
@@ -90,6 +97,7 @@ struct BwdArgs {
     void* h16[4];         // q, k, v, dO as fp16, [B,S,H,d]
     unsigned* amax_bits;  // [4] max |x| of q, k, v, dO (float bits)
     int* exps;            // [8] scale exponents: q, k, v, dO, dS
+    int accum;            // ring step: add dK, dV into the fp32 dk, dv instead of writing them
 };
 
 // Workspace layout of st_attn_bwd (each piece 256-byte aligned).
@@ -102,9 +110,14 @@ BwdWorkspace bwd_workspace_layout(int64_t rows, int d, int dtype);
 int launch_fwd_simt(const SegTable& t, const AttnArgs& a, int dtype, void* stream);
 // Query tiles [t0, t1) of the layout's 256-row tiles (t1 < 0: all of them).
 int launch_fwd_tc(const st_layout& L, const AttnArgs& a, void* stream, bool* handled, int t0 = 0, int t1 = -1);
+// Ring step: the query rows of layout Lq (q, out, lse) against the keys of
+// layout Lkv (k, v); the two may be different shards held as separate buffers.
+int launch_fwd_tc2(const st_layout& Lq, const st_layout& Lkv, const AttnArgs& a, void* stream, int t0 = 0,
+                   int t1 = -1);
 int fwd_tc_tile_rows();
 int launch_bwd_simt(const SegTable& t, const BwdArgs& a, int dtype, void* stream);
 int launch_bwd_tc(const st_layout& L, const BwdArgs& a, void* stream, bool* handled);
+int launch_bwd_tc2(const st_layout& Lq, const st_layout& Lkv, const BwdArgs& a, void* stream);
 // Device error word of the tensor-core kernels (1 after a bounded wait gave
 // up, -1 if it could not be read); clear resets it.
 int fwd_tc_device_error(bool clear);
@@ -131,8 +144,9 @@ int launch_merge(int D, int B, int H, int64_t S, int d, const float* part_out,
 int launch_bwd_preprocess(const BwdArgs& a, int64_t S, int dtype, void* stream);
 // fp32 inputs: lse and Delta of every row recomputed in double
 int launch_rowstats_f64(const SegTable& t, const BwdArgs& a, void* stream);
-// bf16 inputs: max |x| and the scaled fp16 copies of q, k, v, dO
-int launch_fp16_copies(const BwdArgs& a, int64_t S, void* stream);
+// bf16 inputs: max |x| and the scaled fp16 copies of q, k, v, dO (q, dO of
+// Sq rows, k, v of Skv rows)
+int launch_fp16_copies(const BwdArgs& a, int64_t S, void* stream, int64_t Skv = -1);
 // One bf16 tensor -> exact fp16 copy scaled by 2^-exps[0] (forward: V)
 int launch_fp16_copy1(const void* src, void* dst, int64_t elems, unsigned* amax_bits, int* exps,
                       void* stream);

@@ -104,7 +104,8 @@ struct FwdParams {
     CUtensorMap tq;
     CUtensorMap tk;
     CUtensorMap tv;
-    SegTable tab;              // query tiles of kNQ * kM rows
+    SegTable tab;              // query tiles of kNQ * kM rows (q, out, lse)
+    SegTable kvtab;            // the keys (k, v): the same layout, or in a ring step another shard
     const void* q;             // bf16 [B,S,H,D] (read directly when Q lives in TMEM)
     void* out;                 // bf16, or fp32 when out_f32
     float* lse;
@@ -113,6 +114,13 @@ struct FwdParams {
     int causal;
     int out_f32;
     const int* exps;           // exps[0]: v16 = v * 2^-exps[0]
+    // partials mode: per-KV-shard (O_j normalised, lse_j), [D,B,S,H,d] / [D,B,H,S]
+    float* part_out;
+    float* part_lse;
+    // ring step: running state (fp32 out and lse of the query rows) that this
+    // launch's result is merged into by the log-sum-exp rule, or nullptr
+    const float* prev_out;
+    const float* prev_lse;
     int use_order;             // causal: CTAs take tiles heaviest first
     int tile0;                 // first query tile of this launch (without an order)
     uint16_t order[kMaxOrder];
@@ -156,8 +164,20 @@ __device__ __forceinline__ int half_kind(int causal, int nat0, int nq, int natk,
 
 // kSplit: compiled with the hi/lo path for partial tiles (causal masks or
 // ragged shards); layouts whose tiles are all full use the kernel without it.
-template <int D, bool kSplit>
+// kMode: what the kernel writes.
+//   kFused    out, lse of the whole ring (the running state carried across KV shards)
+//   kParts    the partials mode -- instead of carrying the running state from one
+//             KV shard to the next, the state is normalised and written out at the
+//             end of every KV shard (O_j / l_j and lse_j = m_j + ln l_j: what one
+//             ring step hands to the merge) and restarted; a shard with no visible
+//             key gives O_j = 0 and lse_j = -inf.  Compiled with kSplit.
+//   kMerge    a ring step: out, lse of this launch's keys merged by the log-sum-exp
+//             rule into the running state prev_out, prev_lse.  Compiled with kSplit.
+enum { kFused = 0, kParts = 1, kMerge = 2 };
+
+template <int D, bool kSplit, int kMode>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p) {
+    static_assert(kSplit || kMode == kFused, "partials and ring steps walk the ring with the split kernel");
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -258,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             }
             int j = 0;
             bool ok = true;
-            ring_walk<kN>(p.tab, qt.shard, [&](int, int kv0, int nk, int natk, bool) {
+            ring_walk<kN>(p.kvtab, qt.shard, [&](int, int kv0, int nk, int natk, bool) {
                 if (!ok || !active(nk, natk)) return;
                 const int s = j % C::kStages;
                 if (j >= C::kStages) ok = mbar_wait(bar_e(s), ((j / C::kStages) - 1) & 1, abort_flag);
@@ -320,13 +340,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             // + P_lo (both fp16, P_lo in the upper 64 columns of the S region)
             // and a second MMA adds P_lo V.
             // (part 0: keys 0-63, part 1: keys 64-127, part -1: all keys)
-            auto issue_pv = [&](int t, uint64_t vd, int jj, bool split, int part) {
+            // `fresh`: O_t starts from zero with this tile (the first tile
+            // overall; in the partials mode the first tile of every KV shard)
+            auto issue_pv = [&](int t, uint64_t vd, bool fresh, bool split, int part) {
                 const uint32_t tS = tmem + C::s_col(t), tO = tmem + C::o_col(t);
                 const int k0 = part == 1 ? kN / 32 : 0, k1 = part == 0 ? kN / 32 : kN / 16;
 #pragma unroll
                 for (int kk = 0; kk < kN / 16; ++kk)
                     if (kk >= k0 && kk < k1)
-                        mma_ts(tO, tS + kk * 8, vd + (uint64_t)(kk * 128), idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                        mma_ts(tO, tS + kk * 8, vd + (uint64_t)(kk * 128), idesc_o, (!fresh || kk > 0) ? 1u : 0u);
                 if (split) {
 #pragma unroll
                     for (int kk = 0; kk < kN / 16; ++kk)
@@ -338,24 +360,26 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             tc_fence_after();
             int j = 0;
             bool split_prev[kNQ] = {false, false};
+            bool fresh_prev = true;
             // PV_t(j-1) once P_t(j-1) is written (in two halves at d = 64)
             auto pv_when_ready = [&](int t, uint64_t vd, int jj) {
+                const bool fresh = kMode == kParts ? fresh_prev : jj == 0;
                 if constexpr (C::kHalfP) {
                     ok = mbar_wait(bar_pa(t), jj & 1, abort_flag);
                     if (!ok) return;
                     tc_fence_after();
-                    issue_pv(t, vd, jj, split_prev[t], 0);
+                    issue_pv(t, vd, fresh, split_prev[t], 0);
                 }
                 ok = mbar_wait(bar_p(t), jj & 1, abort_flag);
                 if (!ok) return;
                 tc_fence_after();
-                issue_pv(t, vd, jj, split_prev[t], C::kHalfP ? 1 : -1);
+                issue_pv(t, vd, fresh, split_prev[t], C::kHalfP ? 1 : -1);
             };
             // One KV tile.  A tcgen05.commit costs the issuing thread about as
             // much as an MMA, so there are three per tile: S_0, S_1 (each also
             // covers the previous PV of its half, which the softmax relies on
             // before rescaling O) and the stage release.
-            auto step = [&](bool split0, bool split1) {
+            auto step = [&](bool split0, bool split1, bool fresh) {
                 const int s = j % C::kStages;
                 const uint64_t kd = kdesc + (uint64_t)(s * (C::kTileBytes >> 4));
                 ok = mbar_wait(bar_kv(s), (j / C::kStages) & 1, abort_flag);
@@ -377,17 +401,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
                 split_prev[0] = split0;
                 split_prev[1] = split1;
+                fresh_prev = fresh;
                 ++j;
             };
             if constexpr (!kSplit) {
                 // every tile full and visible: the KV tiles are just counted
-                const int nkv = p.tab.S / kN;
-                for (int jj = 0; jj < nkv && ok; ++jj) step(false, false);
+                const int nkv = p.kvtab.S / kN;
+                for (int jj = 0; jj < nkv && ok; ++jj) step(false, false, jj == 0);
             } else {
-                ring_walk<kN>(p.tab, qt.shard, [&](int, int, int nk, int natk, bool) {
+                int prev_shard = -1;
+                ring_walk<kN>(p.kvtab, qt.shard, [&](int js, int, int nk, int natk, bool) {
                     if (!ok || !active(nk, natk)) return;
                     step(half_kind(causal, nat_h[0], nq_h[0], natk, nk) == kPartial,
-                         half_kind(causal, nat_h[1], nq_h[1], natk, nk) == kPartial);
+                         half_kind(causal, nat_h[1], nq_h[1], natk, nk) == kPartial, js != prev_shard);
+                    prev_shard = js;
                 });
             }
             if (ok && j > 0) {
@@ -459,11 +486,63 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 tmem_st16(tO + D, r);
             }
         };
-        auto step = [&](int nk, int natk) {
+        // Partials mode: normalise and write this half's state as the partial of
+        // KV shard js (have = false: the shard had no tile for this CTA, so the
+        // partial is empty: O = 0, lse = -inf).  With have, O_t must hold every
+        // PV product of the shard (the caller has waited for them).
+        auto emit_part = [&](int js, bool have) {
+            float lsum = 0.f;
+            if (have) {
+                if constexpr (C::kSumCol) {
+                    uint32_t r[16];
+                    tmem_ld16(tO + D, r);
+                    tmem_wait_ld();
+                    lsum = __uint_as_float(r[0]);
+                } else {
+                    lsum = l;
+                }
+            }
+            const float inv = lsum > 0.f ? ldexpf(1.f, p.exps[0]) / lsum : 0.f;
+            const int64_t grow = qt.row0 + kM * t + row;
+            float* dst = p.part_out + ((((int64_t)js * p.B + b) * p.tab.S + grow) * H + h) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                if (have) {
+                    tmem_ld32(tO + c * 32, r);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = 0u;
+                }
+                if (row < nq) {
+                    float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                            __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+                }
+            }
+            if (row < nq)
+                p.part_lse[(((int64_t)js * p.B + b) * H + h) * p.tab.S + grow] =
+                    lsum > 0.f ? (m + log2f(lsum)) * kLn2 : -INFINITY;
+        };
+        int cur_shard = -1;   // partials mode: the KV shard whose state O_t, m, l hold
+        auto step = [&](int js, int nk, int natk) {
             if (!ok || !active(nk, natk)) return;
             ok = __all_sync(0xffffffffu, mbar_wait(bar_s(t), j & 1, abort_flag));
             if (!ok) return;
             tc_fence_after();
+            if constexpr (kMode == kParts) {
+                if (js != cur_shard) {
+                    // first tile of a new KV shard: S_t's completion also covers
+                    // every PV of the previous shard, so O_t holds its whole sum
+                    if (cur_shard >= 0) emit_part(cur_shard, true);
+                    m = -INFINITY;
+                    l = 0.f;
+                    cur_shard = js;
+                }
+            }
             const int kind = half_kind(causal, nat_h[t], nq, natk, nk);
             bool resc = false;
             float alpha = 1.f;
@@ -590,13 +669,23 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         };
         if constexpr (!kSplit) {
             // every tile full and visible (the issuer counts them the same way)
-            const int nkv = p.tab.S / kN;
-            for (int jj = 0; jj < nkv && ok; ++jj) step(kN, 0);
+            const int nkv = p.kvtab.S / kN;
+            for (int jj = 0; jj < nkv && ok; ++jj) step(0, kN, 0);
         } else {
-            ring_walk<kN>(p.tab, qt.shard, [&](int, int, int nk, int natk, bool) { step(nk, natk); });
+            ring_walk<kN>(p.kvtab, qt.shard, [&](int js, int, int nk, int natk, bool last) {
+                step(js, nk, natk);
+                if constexpr (kMode == kParts) {
+                    if (ok && last && cur_shard != js) emit_part(js, false);
+                }
+            });
         }
         if (ok && j > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_o(t), 0, abort_flag));
-        if (ok) {
+        if constexpr (kMode == kParts) {
+            if (ok && cur_shard >= 0) {
+                tc_fence_after();
+                emit_part(cur_shard, true);
+            }
+        } else if (ok) {
             tc_fence_after();
             if constexpr (C::kSumCol) {   // l = sum_j P_ij from O's extra column
                 uint32_t r[16];
@@ -605,26 +694,59 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 l = j > 0 ? __uint_as_float(r[0]) : 0.f;
             }
             // O holds P (V * 2^-e_v): undo the fp16 scaling of V with the normalisation
-            const float inv = l > 0.f ? ldexpf(1.f, p.exps[0]) / l : 0.f;
+            float inv = l > 0.f ? ldexpf(1.f, p.exps[0]) / l : 0.f;
             const int64_t grow = qt.row0 + kM * t + row;
             const int64_t off = (((int64_t)b * p.tab.S + grow) * H + h) * D;
+            const int64_t lse_at = ((int64_t)b * H + h) * p.tab.S + grow;
+            float lse_out = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            // Ring step: merge with the running state (O_p, lse_p) by the log-sum-exp
+            // rule, L = log(e^lse_p + e^lse), O = e^(lse_p - L) O_p + e^(lse - L) O.
+            float w_prev = 0.f;
+            if (kMode == kMerge && row < nq) {
+                const float lp = p.prev_lse[lse_at];
+                const float mx = fmaxf(lp, lse_out);
+                if (mx == -INFINITY) {
+                    inv = 0.f;
+                } else {
+                    const float a = exp2f((lp - mx) * kLog2e), c = exp2f((lse_out - mx) * kLog2e);
+                    const float tot = a + c;
+                    w_prev = a / tot;
+                    inv *= c / tot;
+                    lse_out = mx + logf(tot);
+                }
+            }
+            const float* prow = p.prev_out + (kMode == kMerge ? off : 0);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tO + c * 32, r);
                 tmem_wait_ld();
+                if (kMode == kMerge && w_prev > 0.f) {
+                    const float4* p4 = reinterpret_cast<const float4*>(prow + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 x = p4[i];
+                        r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) * inv + w_prev * x.x);
+                        r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) * inv + w_prev * x.y);
+                        r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) * inv + w_prev * x.z);
+                        r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) * inv + w_prev * x.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * inv);
+                }
                 if (row < nq) {
                     if (p.out_f32) {
                         float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off + c * 32);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            d4[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                                __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+                            d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
                     } else {
                         uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+                            pk[i] = pack_bf16(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
                         uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + off + c * 32);
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
@@ -632,8 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     }
                 }
             }
-            if (row < nq)
-                p.lse[((int64_t)b * H + h) * p.tab.S + grow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            if (row < nq) p.lse[lse_at] = lse_out;
         }
     }
 
@@ -681,15 +802,16 @@ bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int d,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool kSplit>
-int launch_t(const st_layout& L, const AttnArgs& a, void* stream, int t0, int t1) {
+template <int D, bool kSplit, int kMode>
+int launch_t(const st_layout& L, const st_layout& Lkv, const AttnArgs& a, void* stream, int t0, int t1) {
     using C = Cfg<D>;
     FwdParams p;
-    const int S = (int)L.S;
-    if (!make_map(&p.tq, a.q, a.B, S, a.H, D) || !make_map(&p.tk, a.k, a.B, S, a.H, D) ||
-        !make_map(&p.tv, a.v16, a.B, S, a.H, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
+    const int S = (int)L.S, Skv = (int)Lkv.S;
+    if (!make_map(&p.tq, a.q, a.B, S, a.H, D) || !make_map(&p.tk, a.k, a.B, Skv, a.H, D) ||
+        !make_map(&p.tv, a.v16, a.B, Skv, a.H, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
         return (int)cudaErrorInvalidValue;
     fill_segtable(L, kNQ * kM, &p.tab);
+    fill_segtable(Lkv, kN, &p.kvtab);
     if (t1 < 0 || t1 > p.tab.ntiles) t1 = p.tab.ntiles;
     if (t0 < 0) t0 = 0;
     if (t0 >= t1) return 0;
@@ -720,11 +842,15 @@ int launch_t(const st_layout& L, const AttnArgs& a, void* stream, int t0, int t1
     p.out_f32 = a.out_dtype == ST_DTYPE_F32 ? 1 : 0;
     p.exps = a.exps;
     p.lse = a.lse;
+    p.part_out = a.part_out;
+    p.part_lse = a.part_lse;
+    p.prev_out = a.prev_out;
+    p.prev_lse = a.prev_lse;
     p.B = a.B;
     p.H = a.H;
     p.scale_log2 = a.scale * kLog2e;
     p.causal = a.causal;
-    auto kern = fwd_tc_kernel<D, kSplit>;
+    auto kern = fwd_tc_kernel<D, kSplit, kMode>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return (int)e;
     dim3 grid(t1 - t0, a.B * a.H);
@@ -736,15 +862,32 @@ int launch_t(const st_layout& L, const AttnArgs& a, void* stream, int t0, int t1
 
 int fwd_tc_tile_rows() { return kNQ * kM; }
 
+int launch_fwd_tc2(const st_layout& L, const st_layout& Lkv, const AttnArgs& a, void* stream, int t0, int t1) {
+    // partial (query half, KV tile) pairs exist under causal masking or when a
+    // KV segment is not a multiple of the 128-key tile
+    bool split = a.causal != 0;
+    for (size_t s = 0; s + 1 < Lkv.seg_buf.size(); ++s)
+        split |= ((Lkv.seg_buf[s + 1] - Lkv.seg_buf[s]) % kN) != 0;
+    if (a.part_out) {
+        // partials: the ring walk of the split kernel, state written per KV shard
+        return a.d == 64 ? launch_t<64, true, kParts>(L, Lkv, a, stream, t0, t1)
+                         : launch_t<128, true, kParts>(L, Lkv, a, stream, t0, t1);
+    }
+    if (a.prev_out) {
+        // ring step merged into the running state
+        return a.d == 64 ? launch_t<64, true, kMerge>(L, Lkv, a, stream, t0, t1)
+                         : launch_t<128, true, kMerge>(L, Lkv, a, stream, t0, t1);
+    }
+    if (a.d == 64)
+        return split ? launch_t<64, true, kFused>(L, Lkv, a, stream, t0, t1)
+                     : launch_t<64, false, kFused>(L, Lkv, a, stream, t0, t1);
+    return split ? launch_t<128, true, kFused>(L, Lkv, a, stream, t0, t1)
+                 : launch_t<128, false, kFused>(L, Lkv, a, stream, t0, t1);
+}
+
 int launch_fwd_tc(const st_layout& L, const AttnArgs& a, void* stream, bool* handled, int t0, int t1) {
     *handled = true;
-    // partial tiles exist under causal masking or when a segment is not a
-    // multiple of the 128-row tile
-    bool split = a.causal != 0;
-    for (size_t s = 0; s + 1 < L.seg_buf.size(); ++s)
-        split |= ((L.seg_buf[s + 1] - L.seg_buf[s]) % kN) != 0;
-    if (a.d == 64) return split ? launch_t<64, true>(L, a, stream, t0, t1) : launch_t<64, false>(L, a, stream, t0, t1);
-    return split ? launch_t<128, true>(L, a, stream, t0, t1) : launch_t<128, false>(L, a, stream, t0, t1);
+    return launch_fwd_tc2(L, L, a, stream, t0, t1);
 }
 
 int fwd_tc_device_error(bool clear) {

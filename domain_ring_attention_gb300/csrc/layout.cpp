@@ -104,4 +104,20 @@ void fill_segtable(const st_layout& L, int tile_rows, SegTable* t) {
     for (int r = 0; r <= L.D; ++r) t->shard_seg[r] = L.shard_seg[r];
 }
 
+st_layout shard_layout(const st_layout& L, int r) {
+    st_layout s;
+    s.D = 1;
+    s.zigzag = L.zigzag;
+    s.S = L.lens[r];
+    s.lens = {L.lens[r]};
+    s.off = {0, L.lens[r]};
+    for (int g = L.shard_seg[r]; g < L.shard_seg[r + 1]; ++g) {
+        s.seg_buf.push_back(L.seg_buf[g] - L.off[r]);
+        s.seg_nat.push_back(L.seg_nat[g]);
+    }
+    s.seg_buf.push_back(L.lens[r]);
+    s.shard_seg = {0, L.shard_seg[r + 1] - L.shard_seg[r]};
+    return s;
+}
+
 }  // namespace st

@@ -179,16 +179,22 @@ int st_attn_fwd_noalloc(const st_layout_t* layout, int B, int H, int d, int dtyp
                         float scale, const void* q, const void* k, const void* v, int out_dtype,
                         void* out, float* lse, void* stream);
 
-/* Forward that stops short of the merge: for every query row and every KV
- * shard j it writes the partial (O_j normalised by its own sum, lse_j) over
- * the keys of shard j only -- what each ring step would hand to the merge.
- * A partial with no visible key has O_j = 0 and lse_j = -inf.
+/* Forward that stops short of the merge (ShardTensor summary, section 4,
+ * ring attention: each query shard meets every KV shard and the partial
+ * results are combined): for every query row and every KV shard j it writes
+ * the partial (O_j normalised by its own sum, lse_j) over the keys of shard j
+ * only -- what each ring step hands to the merge.  A partial with no visible
+ * key has O_j = 0 and lse_j = -inf.
  *   partial_out : [D,B,S,H,d] fp32;  partial_lse : [D,B,H,S] fp32.
- * st_attn_merge of these partials equals st_attn_fwd up to rounding. */
+ *   workspace   : as st_attn_fwd (pass 0): bf16 inputs run the tensor-core
+ *                 forward, which restarts its running state at every KV
+ *                 shard and writes it out; fp32 needs none (NULL / 0).
+ * st_attn_merge of these partials equals st_attn_fwd up to rounding.
+ * Errors: as st_attn_fwd. */
 int st_attn_fwd_partials(const st_layout_t* layout, int B, int H, int d, int dtype,
                          int causal, float scale, const void* q, const void* k,
                          const void* v, float* partial_out, float* partial_lse,
-                         void* stream);
+                         void* workspace, size_t ws_bytes, void* stream);
 
 /* Log-sum-exp merge of D partials (the ring-attention combine step):
  *   L = log sum_j exp(lse_j);  out = sum_j exp(lse_j - L) O_j.
@@ -222,6 +228,117 @@ int st_attn_bwd(const st_layout_t* layout, int B, int H, int d, int dtype, int c
                 const void* out, int out_dtype, const float* lse, const void* dout,
                 int grad_dtype, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                 void* stream);
+
+/*
+ * Ring attention across ranks (ShardTensor summary, section 4, ring
+ * attention; TSP summary, section 2, attention layer, for the zigzag
+ * re-partition).  Rank r keeps the query rows of shard r of the layout; the
+ * K/V shards travel round a ring of ranks, so that at step t = 0 .. D-1 rank
+ * r holds the K/V of shard (r - t) mod D -- its own at step 0, then each step
+ * the block its left neighbour held -- and folds that shard's partial result
+ * into its running result by the log-sum-exp rule.  In training the K/V
+ * shards travel with fp32 dK/dV accumulators, to which every rank adds its
+ * queries' contributions, and one more hop after the last step brings them to
+ * the shard's owner.  The causal mask follows the natural positions of both
+ * shards.  Only bf16 inputs (the tensor-core path); a shard's tensors are
+ * [B, L_r, H, d] (q, k, v, out, dout) and [B, H, L_r] (lse), contiguous, in the
+ * rank's buffer order (with zigzag, chunk r then chunk 2D-1-r).
+ */
+
+/* Workspace bytes for any pair of shards of the layout (sized by the longest
+ * shard): which = 0 st_ring_fwd_step, 1 st_ring_bwd_step, 2 st_ring_fwd_local,
+ * 3 st_ring_bwd_local. */
+int st_ring_workspace_size(const st_layout_t* layout, int B, int H, int d, int which, size_t* bytes);
+
+/* One forward step of rank q_shard: its query rows q against the K/V block of
+ * shard kv_shard that it holds at this step.  With prev_out / prev_lse NULL
+ * (the first step) out, lse = this block's partial (O normalised by its own
+ * sum, lse = log of that sum; no visible key: O = 0, lse = -inf); otherwise
+ * the partial is merged with the running state (prev_out fp32 [B,L_q,H,d],
+ * prev_lse [B,H,L_q]) into out, lse:  L = log(e^lse_prev + e^lse_blk),
+ * out = e^(lse_prev - L) prev_out + e^(lse_blk - L) O_blk.  out and lse may
+ * alias prev_out and prev_lse (fp32 out).
+ *   q        : [B, L_q, H, d] bf16;  k, v : [B, L_kv, H, d] bf16.
+ *   out_dtype: ST_DTYPE_F32 (the running state) or ST_DTYPE_BF16 (a last step).
+ *   dtype    : ST_DTYPE_BF16.
+ *   workspace: st_ring_workspace_size(which = 0) bytes of device memory.
+ * One fp16 copy of v and the fused kernel on `stream`.
+ * Errors: as st_attn_fwd, plus ST_ERR_INVALID_ARG for a shard index out of
+ * range and ST_ERR_NULL when only one of prev_out, prev_lse is given. */
+int st_ring_fwd_step(const st_layout_t* layout, int q_shard, int kv_shard, int B, int H, int d, int dtype,
+                     int causal, float scale, const void* q, const void* k, const void* v,
+                     const float* prev_out, const float* prev_lse, int out_dtype, void* out, float* lse,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* One backward step of rank q_shard holding shard kv_shard's K/V and their
+ * travelling gradient accumulators: adds this block's contributions
+ *   dV_kv += P^T dO,  dK_kv += scale dS^T Q,  dQ_q += scale dS K
+ * (P = exp(scale QK^T - lse), dS = P o (dO V^T - Delta), Delta = rowsum(dO o
+ * out)) to the fp32 dk, dv [B,L_kv,H,d] and dq [B,L_q,H,d].  first_q = 1
+ * zeroes dq first (the rank's first step).  out: the rank's forward output
+ * (bf16 or fp32, out_dtype), lse its fp32 lse.  dtype: ST_DTYPE_BF16.
+ * workspace: st_ring_workspace_size(which = 1) bytes.
+ * Errors: as st_attn_bwd, plus ST_ERR_INVALID_ARG for a shard index out of
+ * range. */
+int st_ring_bwd_step(const st_layout_t* layout, int q_shard, int kv_shard, int B, int H, int d, int dtype,
+                     int causal, float scale, const void* q, const void* k, const void* v, const void* out,
+                     int out_dtype, const float* lse, const void* dout, int first_q, float* dq, float* dk,
+                     float* dv, void* workspace, size_t ws_bytes, void* stream);
+
+/* The whole ring forward with the D ranks held on this one GPU: host arrays of
+ * D device pointers give rank r's q, k, v (its shard) and its outputs out
+ * ([B,L_r,H,d], out_dtype) and lse ([B,H,L_r]).  The K/V blocks pass from
+ * rank to rank by device-to-device copies on copy_stream (a stream other than
+ * `stream`) into two receive buffers per rank in the workspace, each step's
+ * copies running while the previous blocks are computed on `stream`.  When
+ * `stream` completes, every rank's out and lse hold its queries' attention
+ * over the whole sequence.  workspace: st_ring_workspace_size(which = 2).
+ * Errors: as st_ring_fwd_step, plus ST_ERR_INVALID_ARG when copy_stream is
+ * NULL or equal to stream. */
+int st_ring_fwd_local(const st_layout_t* layout, int B, int H, int d, int causal, float scale,
+                      const void* const* q, const void* const* k, const void* const* v, int out_dtype,
+                      void* const* out, float* const* lse, void* workspace, size_t ws_bytes, void* stream,
+                      void* copy_stream);
+
+/* The whole ring backward with the D ranks on this one GPU: rank r's q, k, v,
+ * out (out_dtype), lse, dout in, fp32 dq, dk, dv of its shard out.  K and V
+ * pass on while a step computes; the dK/dV accumulators pass on after it has
+ * added to them, and after the last step they reach their owner's dk, dv.
+ * workspace: st_ring_workspace_size(which = 3).  Errors: as
+ * st_ring_bwd_step, plus ST_ERR_INVALID_ARG for copy_stream. */
+int st_ring_bwd_local(const st_layout_t* layout, int B, int H, int d, int causal, float scale,
+                      const void* const* q, const void* const* k, const void* const* v, const void* const* out,
+                      int out_dtype, const float* const* lse, const void* const* dout, float* const* dq,
+                      float* const* dk, float* const* dv, void* workspace, size_t ws_bytes, void* stream,
+                      void* copy_stream);
+
+/* Backward preprocess on its own: Delta[b,h,i] = sum_c dout[b,i,h,c] *
+ * out[b,i,h,c] in fp32 -- the row sums of dO o O that the backward subtracts
+ * from dP (the gradient of the softmax).  A ring backward computes them once
+ * per rank, before its steps.
+ *   out  : [B,S,H,d] in out_dtype (dtype or ST_DTYPE_F32);  dout : [B,S,H,d]
+ *   dtype;  delta : [B,H,S] fp32.  One launch, HBM-bound.
+ * Errors: ST_ERR_NULL, ST_ERR_INVALID_ARG, ST_ERR_UNSUPPORTED,
+ * ST_ERR_MISALIGNED, ST_ERR_NOT_DEVICE, ST_ERR_CUDA. */
+int st_attn_bwd_delta(int B, int H, int64_t S, int d, int dtype, const void* out, int out_dtype,
+                      const void* dout, float* delta, void* stream);
+
+/* fp32 accumulator -> dst_dtype (ST_DTYPE_BF16: rounded to nearest even;
+ * ST_DTYPE_F32: copied): n elements, the conversion the backward applies to
+ * its dQ accumulator, also the last step of an fp32 ring result.  One
+ * launch, HBM-bound.  Errors: ST_ERR_NULL, ST_ERR_INVALID_ARG,
+ * ST_ERR_UNSUPPORTED, ST_ERR_MISALIGNED, ST_ERR_NOT_DEVICE, ST_ERR_CUDA. */
+int st_convert_f32(int64_t n, const float* src, void* dst, int dst_dtype, void* stream);
+
+/* The exact fp16 operand copy the tensor-core kernels run on: dst = src *
+ * 2^-e in fp16 for n bf16 values (n a multiple of 8), e chosen from max|src|
+ * so that max|src| * 2^-e lies in [2^13, 2^14) -- bf16's 8 significant bits
+ * fit in fp16's 11, so every value within 2^-27 of the maximum is copied
+ * exactly.  exps[0] receives e (device int); scratch: 16 device bytes for the
+ * maximum.  Two launches (max, copy), HBM-bound.
+ * Errors: ST_ERR_NULL, ST_ERR_INVALID_ARG, ST_ERR_MISALIGNED,
+ * ST_ERR_NOT_DEVICE, ST_ERR_CUDA. */
+int st_fp16_scaled_copy(int64_t n, const void* src, void* dst, int* exps, void* scratch, void* stream);
 
 /* Reorder rows between buffer order and natural sequence order:
  *   to_natural = 1 : out[:, pos(t)] = in[:, t]   (buffer -> natural)

@@ -219,3 +219,29 @@ def test_bounded_wait_selftest_rejects_bad_limits(lib):
     assert lib.st_selftest_bounded_wait(0, None) == -8
     assert lib.st_selftest_bounded_wait(-5, None) == -8
     assert lib.st_selftest_bounded_wait(5 * 10 ** 9, None) == -8
+
+
+def test_ring_entry_points_check_arguments_on_the_host(lib):
+    lay = st.Layout([256, 128, 384], True)
+    n = ctypes.c_size_t()
+    for which in range(4):
+        assert lib.st_ring_workspace_size(lay.handle, 1, 2, 128, which, ctypes.byref(n)) == 0 and n.value > 0
+    assert lib.st_ring_workspace_size(lay.handle, 1, 2, 128, 4, ctypes.byref(n)) == -8
+    assert lib.st_ring_workspace_size(lay.handle, 1, 2, 96, 0, ctypes.byref(n)) == -3
+    P = ctypes.c_void_p
+    good = P(0x10000)
+    args = lambda qs, ks, dt: (lay.handle, qs, ks, 1, 2, 128, dt, 1, 0.0, good, good, good, None, None, 0, good,
+                               good, good, 1 << 30, None)
+    assert lib.st_ring_fwd_step(*args(3, 0, 1)) == -8          # shard index out of range
+    assert lib.st_ring_fwd_step(*args(0, -1, 1)) == -8
+    assert lib.st_ring_fwd_step(*args(0, 1, 0)) == -3          # fp32: not a ring-step dtype
+    a = list(args(0, 1, 1))
+    a[12] = good                                               # prev_out without prev_lse
+    assert lib.st_ring_fwd_step(*a) == -1
+    a = list(args(0, 1, 1))
+    a[18] = 16                                                 # workspace too small
+    assert lib.st_ring_fwd_step(*a) == -5
+    arr = (P * 3)(good, good, good)
+    # copy stream missing
+    assert lib.st_ring_fwd_local(lay.handle, 1, 2, 128, 1, 0.0, arr, arr, arr, 1, arr, arr, good, 1 << 40,
+                                 None, None) == -8

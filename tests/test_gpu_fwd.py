@@ -6,7 +6,7 @@ import torch
 
 import domain_ring_attention_gb300 as st
 from domain_ring_attention_gb300.workloads import WORKLOADS, Workload, make_inputs, sample_rows
-from gpu_common import assert_close, assert_lse, check_full, check_rows, f64, run_case
+from gpu_common import assert_close, assert_lse, assert_no_device_error, check_full, check_rows, f64, run_case
 from oracle import attention as oa
 from oracle import layout as ol
 
@@ -68,23 +68,39 @@ def test_repeated_calls_are_identical():
 
 # ------------------------------------------------------------- partials, merge, permute
 
+PARTIAL_LAYOUTS = [
+    ((100, 150, 130, 132), False, False),
+    ((2, 6, 250, 32), True, True),
+    ((128, 128, 128, 128), True, True),
+    ((512, 256, 768, 512), True, True),
+    ((300,), False, True),
+    ((256, 256, 256, 256), False, False),     # every tile full
+    ((1, 7, 64, 129), False, True),
+]
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("lens,zigzag,causal", [((100, 150, 130, 132), False, False),
-                                                ((2, 6, 250, 32), True, True),
-                                                ((128, 128, 128, 128), True, True)])
-def test_partials_match_oracle_and_merge_to_fused(lens, zigzag, causal, dtype):
-    wl = Workload("part", B=2, H=2, d=64, lens=lens, causal=causal, zigzag=zigzag, dtype=dtype)
-    q, k, v = (x.cuda() for x in make_inputs(wl, seed=11))
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("lens,zigzag,causal", PARTIAL_LAYOUTS)
+def test_partials_match_oracle_and_merge_to_attention(lens, zigzag, causal, d, dtype):
+    """The partials mode (bf16: the tensor-core forward writing and restarting its state at every KV shard)
+    against the oracle's per-(query row, KV shard) partials, and the standalone merge of those partials
+    against the oracle's full attention."""
+    wl = Workload("part", B=2, H=2, d=d, lens=lens, causal=causal, zigzag=zigzag, dtype=dtype)
+    q, k, v = (x.cuda() for x in make_inputs(wl, seed=11 + d))
     lay = st.Layout(lens, zigzag)
     po, pl = st.st_attn_fwd_partials(lay, q, k, v, causal=causal)
-    ro, rl = oa.ring_partials(f64(q), f64(k), f64(v), lens, zigzag, causal)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    Q, K, V = f64(q), f64(k), f64(v)
+    ro, rl = oa.ring_partials(Q, K, V, lens, zigzag, causal)
     assert_close(f64(po), ro, dtype, "partial_out")
     assert_lse(f64(pl), rl, dtype, "partial_lse")
-    mo, ml = st.st_attn_merge(po, pl, out_dtype=q.dtype)
-    fo, fl = st.st_attn_fwd(lay, q, k, v, causal=causal)
+    mo, ml = st.st_attn_merge(po, pl, out_dtype=torch.float32)
     torch.cuda.synchronize()
-    assert_close(f64(mo), f64(fo), dtype, "merged vs fused")
-    assert_close(f64(ml), f64(fl), dtype, "merged lse vs fused")
+    fo, fl = oa.forward(Q, K, V, lens, zigzag, causal)
+    assert_close(f64(mo), fo, dtype, "merged out")
+    assert_lse(f64(ml), fl, dtype, "merged lse")
 
 
 @pytest.mark.parametrize("d", [64, 128])
