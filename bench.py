@@ -37,12 +37,12 @@ from domain_ring_attention_gb300.workloads import WORKLOADS, make_inputs
 METRIC = "ring-attention fwd/bwd TFLOP/s (bf16, S=65536) and % of GB300 dense-BF16 peak"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
-# dram bytes (read + write) per launch of the forward kernel on the default
-# workload, from the committed ncu capture of the kernel version named here
-# (2-head capture scaled by 8 to 16 heads: the traffic is per head); a kernel
-# change without a new capture must drop its entry (traffic is then null).
-NCU_TRAFFIC_BYTES = {"fwd_tc@5875d80": 8 * (50.388224e6 + 0.517888e6)}
-KERNEL_VERSION = "fwd_tc@5875d80"
+# dram bytes (read + write) of one full-size launch of the forward kernel on the
+# default workload (16 heads), from the committed ncu capture of the kernel
+# version named here; a kernel change without a new capture must drop its entry
+# (traffic is then null).
+NCU_TRAFFIC_BYTES = {"fwd_tc@f4d144b": 423702272.0 + 123534080.0}
+KERNEL_VERSION = "fwd_tc@f4d144b"
 DEFAULT_WORKLOAD = "vit4096_s65536"
 
 
