@@ -13,7 +13,9 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "lib", "libst_attn.so")
+# ST_ATTN_LIB may name another build of the same library (e.g. one made with
+# other compiler flags); by default the in-tree build is loaded.
+LIB_PATH = os.environ.get("ST_ATTN_LIB") or os.path.join(_PKG, "lib", "libst_attn.so")
 
 ST_DTYPE_F32 = 0
 ST_DTYPE_BF16 = 1
