@@ -479,6 +479,59 @@ def train_step_tflops(st, world, steps=3, warmup=2, name="train_s32768"):
             "note": "fwd writes fp32 out (the backward's Delta); bwd writes fp32 dq, dk, dv"}
 
 
+def ring_local_tflops(st, world, steps=3, warmup=2, name="train_s32768"):
+    """The ring schedule with every rank's shard on this one GPU (st_ring_fwd_local /
+    st_ring_bwd_local): rank r keeps query shard r, the K/V blocks (in the
+    backward with their dK/dV accumulators) pass from rank to rank by device
+    copies on a second stream while the previous blocks compute.  On one GPU the
+    D ranks' step kernels run one after another, so this measures the ring's
+    per-step kernels and copies, not a multi-GPU ring; the fused kernels are the
+    one-GPU path.  fp32 outputs and gradients."""
+    from domain_ring_attention_gb300 import _lib
+    wl = WORKLOADS[name]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v, do = make_inputs(wl, seed=9, device=dev, with_dout=True)
+    lay = st.Layout(wl.lens, wl.zigzag)
+    off = np.cumsum([0] + list(wl.lens))
+    cut = lambda x: [x[:, off[r]:off[r + 1]].contiguous() for r in range(wl.D)]
+    qs, ks, vs, dos = cut(q), cut(k), cut(v), cut(do)
+    del q, k, v, do
+    wsf = torch.empty(_lib.st_ring_workspace_size(lay, wl.B, wl.H, wl.d, 2), device=dev, dtype=torch.uint8)
+    wsb = torch.empty(_lib.st_ring_workspace_size(lay, wl.B, wl.H, wl.d, 3), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+    copy_stream = torch.cuda.Stream()
+    state = {}
+
+    def fwd():
+        state["o"], state["l"] = _lib.st_ring_fwd_local(lay, qs, ks, vs, causal=wl.causal, out_dtype=torch.float32,
+                                                        stream=stream, copy_stream=copy_stream, workspace=wsf)
+
+    def bwd():
+        _lib.st_ring_bwd_local(lay, qs, ks, vs, state["o"], state["l"], dos, causal=wl.causal, stream=stream,
+                               copy_stream=copy_stream, workspace=wsb)
+
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    tf = tb = 0.0
+    for _ in range(steps):
+        ev[0].record(stream)
+        fwd()
+        ev[1].record(stream)
+        bwd()
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        tf += ev[0].elapsed_time(ev[1])
+        tb += ev[1].elapsed_time(ev[2])
+    tf = max_over_ranks(tf / steps, world)
+    tb = max_over_ranks(tb / steps, world)
+    return {"workload": name, "ranks_on_one_gpu": wl.D, "fwd_tflops": wl.fwd_flops() / (tf * 1e-3) / 1e12,
+            "bwd_tflops": wl.bwd_flops() / (tb * 1e-3) / 1e12, "fwd_ms": tf, "bwd_ms": tb,
+            "note": "ring schedule emulated on one GPU: the D ranks' step kernels run one after another"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -638,10 +691,13 @@ def run_ours(args, rank, world):
     if not args.no_train:
         cool_down()
     train = None if args.no_train else train_step_tflops(st, world)
-    llm7b = None
+    llm7b = ring_local = None
     if not args.no_train and not args.bwd:
         cool_down()
         llm7b = train_step_tflops(st, world, name="llm7b_causal_s131072")
+        if world == 1:
+            cool_down()
+            ring_local = ring_local_tflops(st, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -671,7 +727,7 @@ def run_ours(args, rank, world):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
-            "secondary": {"train": train, "llm7b": llm7b, "merge": merge, "bwd_hbm_steps": hbm_steps, "mufu": mufu, "proj": proj, "mlp": mlp, "conv": conv, "norm": gnorm},
+            "secondary": {"train": train, "llm7b": llm7b, "ring_local": ring_local, "merge": merge, "bwd_hbm_steps": hbm_steps, "mufu": mufu, "proj": proj, "mlp": mlp, "conv": conv, "norm": gnorm},
         }
         print(json.dumps(line), flush=True)
 

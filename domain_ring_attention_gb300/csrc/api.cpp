@@ -21,22 +21,8 @@ int cuda_status(int err) {
     return ST_ERR_CUDA;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// Memory the kernels may read and write: device or managed allocations.  A
-// pointer to ordinary host memory handed to a kernel would fault the GPU, so
-// every entry point checks its device pointers with the runtime, after all its
-// other checks (so argument errors are still reported without a GPU).  NULL
-// is accepted here (optional arguments were checked before).
-bool on_device(const void* p) {
-    if (!p) return true;
-    cudaPointerAttributes at;
-    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
-        cudaGetLastError();   // do not leave the failure to be read as a launch error
-        return false;
-    }
-    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
-}
+using st::aligned16;
+using st::on_device;
 
 template <typename... P>
 bool all_on_device(P... ps) {
@@ -218,6 +204,23 @@ extern "C" int st_gated_mlp(int M, int hidden, int F, const void* x, const void*
 }
 
 namespace st {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Memory the kernels may read and write: device or managed allocations.  A
+// pointer to ordinary host memory handed to a kernel would fault the GPU, so
+// every entry point checks its device pointers with the runtime, after all its
+// other checks (so argument errors are still reported without a GPU).  NULL
+// is accepted here (optional arguments were checked before).
+bool on_device(const void* p) {
+    if (!p) return true;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();   // do not leave the failure to be read as a launch error
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
 
 BwdWorkspace bwd_workspace_layout(int64_t rows, int d, int dtype) {
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };

@@ -72,6 +72,10 @@ struct AttnArgs {
 size_t fwd_workspace_bytes(int64_t rows, int d, int dtype);
 // Records a CUDA error code for st_last_cuda_error and returns ST_ERR_CUDA (0 -> ST_OK).
 int record_cuda_error(int err);
+// Argument checks shared by the entry points: 16-byte alignment, and whether a
+// pointer addresses device (or managed) memory (NULL passes; host-only query).
+bool aligned16(const void* p);
+bool on_device(const void* p);
 
 struct BwdArgs {
     const void* q;

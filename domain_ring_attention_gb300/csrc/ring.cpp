@@ -29,17 +29,8 @@ namespace {
 
 int cuda_status(int err) { return st::record_cuda_error(err); }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-bool on_device(const void* p) {
-    if (!p) return true;
-    cudaPointerAttributes at;
-    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
-}
+using st::aligned16;
+using st::on_device;
 
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 

@@ -95,6 +95,11 @@ def test_vit1024_workload_backward_full():
 
 @pytest.mark.slow
 def test_train_workload_backward_one_head():
+    """The training workload at full size: every gradient element of head (1, 5) against the oracle's full
+    backward, and for head (0, 0) every forward row plus sampled dQ rows and dK / dV key columns (the lead
+    tile, the shard and chunk edges, 256 random) against the oracle's row statistics."""
+    import os
+    from oracle import layout as ol
     wl = WORKLOADS["train_s32768"]
     res = run_case(wl, backward=True)
     b, h = 1, 5
@@ -103,6 +108,31 @@ def test_train_workload_backward_one_head():
     rg = oa.backward(q, k, v, ro, rl, do, wl.lens, wl.zigzag, wl.causal)
     for name, g, r in zip(("dq", "dk", "dv"), res["grads"], rg):
         assert_close(f64(g[b:b + 1, :, h:h + 1]), r, wl.dtype, name, rel_rms=True)
+    b, h = 0, 0
+    S = wl.S
+    Q, K, V, DO = (f64(x[b:b + 1, :, h:h + 1]) for x in res["in"])
+    outs, lses, deltas = oa.row_stats(Q, K, V, DO, wl.lens, wl.zigzag, True,
+                                      workers=max(1, min(16, os.cpu_count() or 1)))
+    assert_close(f64(res["out"][b, :, h]), outs[(0, 0)], "bf16", "out[0,0] (all rows)")
+    pos = ol.natural_positions(list(wl.lens), wl.zigzag)
+    at = np.argsort(pos)
+    lead = at[:128]
+    rest = np.setdiff1d(np.arange(S), lead)
+    sample = np.sort(np.random.default_rng(11).choice(rest, size=256, replace=False))
+    off = ol.shard_offsets(list(wl.lens))
+    mids = [off[r] + wl.lens[r] // 2 for r in range(len(wl.lens))]          # zigzag chunk boundaries
+    edges = np.unique(np.concatenate([[o, o - 1] for o in list(off[1:-1]) + mids] + [[0, S - 1]]))
+    dq, dk, dv = res["grads"]
+    pick = lambda t, idx: f64(t[b, torch.as_tensor(idx, device=t.device), h])
+    rows = np.concatenate([lead, sample])
+    rq = oa.backward_rows(Q, K, V, DO, wl.lens, wl.zigzag, True, np.concatenate([rows, edges]),
+                          heads=[(0, 0)])[(0, 0)]
+    _stratified_check(pick(dq, rows), rq[:len(rows)], 128, S, "dq[0,0]", pick(dq, edges), rq[len(rows):])
+    rk, rv = oa.backward_cols(Q, K, V, DO, wl.lens, wl.zigzag, True, np.concatenate([rows, edges]), lses, deltas)
+    _stratified_check(pick(dk, rows), rk[(0, 0)][:len(rows)], 128, S, "dk[0,0]", pick(dk, edges),
+                      rk[(0, 0)][len(rows):])
+    _stratified_check(pick(dv, rows), rv[(0, 0)][:len(rows)], 128, S, "dv[0,0]", pick(dv, edges),
+                      rv[(0, 0)][len(rows):])
 
 
 def _stratified_check(got, ref, n_lead, n_total, name, extra_got=None, extra_ref=None):

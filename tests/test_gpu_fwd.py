@@ -140,10 +140,19 @@ def test_permute_round_trip(lens, zigzag):
 
 @pytest.mark.slow
 def test_vit4096_workload_sampled_rows():
+    """The ViT 4096^2 workload at full size: 192 sampled rows of three heads, and every one of the
+    65536 rows of head 7 (out and lse) against the oracle."""
+    import os
     wl = WORKLOADS["vit4096_s65536"]
     res = run_case(wl, backward=False)
     rows = sample_rows(wl.S, 192, seed=3)
     check_rows(wl, res, rows, [(0, 0), (0, 7), (0, 15)])
+    h = 7
+    Q, K, V = (f64(x[0:1, :, h:h + 1]) for x in res["in"][:3])
+    outs, lses, _ = oa.row_stats(Q, K, V, np.zeros_like(Q), wl.lens, wl.zigzag, wl.causal,
+                                 workers=max(1, min(16, os.cpu_count() or 1)))
+    assert_close(f64(res["out"][0, :, h]), outs[(0, 0)], wl.dtype, "out[0,7] (all rows)")
+    assert_close(f64(res["lse"][0, h]), lses[(0, 0)], wl.dtype, "lse[0,7] (all rows)")
 
 
 @pytest.mark.slow
