@@ -26,6 +26,7 @@ LAYOUTS = [
     ((256, 256), False, True),
     ((384, 128, 640), False, False),
     ((300,), False, True),
+    ((640, 128, 2, 384, 256, 512, 64, 96), True, True),     # eight ranks, uneven, a 2-row shard
 ]
 
 

@@ -90,7 +90,7 @@ def _worker(rank, world, port, lens, zigzag, causal, queue):
 
 
 @pytest.mark.parametrize("lens,zigzag,causal", [((6, 10), True, True), ((5, 9, 3), False, False),
-                                                ((4, 12, 2), True, True)])
+                                                ((4, 12, 2), True, True), ((2, 8, 4, 6), True, True)])
 def test_ring_schedule_across_processes(lens, zigzag, causal):
     world, port = len(lens), free_port()
     ctx = mp.get_context("spawn")
