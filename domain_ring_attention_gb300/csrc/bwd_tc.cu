@@ -201,13 +201,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     if (threadIdx.x == 0) {
         mbar_init(bar_kv, 1);
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(bar_qf(s), 33);
+            mbar_init(bar_qf(s), 2);     // the TMA bytes' arrival + the producer warp's statistics
             mbar_init(bar_qe(s), 1);
         }
         mbar_init(bar_s, 1);
-        mbar_init(bar_ds, 256);
+        mbar_init(bar_ds, 8);       // one arrival per softmax warp
         mbar_init(bar_it, 1);
-        mbar_init(bar_dqf, 256);
+        mbar_init(bar_dqf, 8);
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -267,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 ls[e * 32 + lane] = nl[e];
                 ls[kT + e * 32 + lane] = nd[e];
             }
-            mbar_arrive(bar_qf(s));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_qf(s));
             ++i;
         });
         if (lane == 0) {
@@ -528,7 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 tmem_ld32(lane_base + C::kColDP + grp * kCols + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(bar_dqf);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_dqf);
             // The reductions go through the TMA: per 32-column chunk the warp
             // writes its 32 rows into a 128-byte-swizzled fp32 tile (rows past
             // the query tile as zeros, which add nothing) and one lane issues a
@@ -598,7 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             tmem_wait_st();
             fence_proxy_async();
             tc_fence_before();
-            mbar_arrive(bar_ds);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_ds);
             ok = __all_sync(0xffffffffu, mbar_wait(bar_it, i & 1, abort_flag));
             if (!ok) return;
             tc_fence_after();

@@ -220,15 +220,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     };
 
     if (threadIdx.x == 0) {
-        mbar_init(bar_q, C::kQTmem ? kNQ * kM : 1);
+        mbar_init(bar_q, C::kQTmem ? kNQ * kM / 32 : 1);     // one arrival per softmax warp
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar_kv(s), 1);
             mbar_init(bar_e(s), 1);
         }
         for (int t = 0; t < kNQ; ++t) {
             mbar_init(bar_s(t), 1);
-            mbar_init(bar_p(t), 128);
-            mbar_init(bar_pa(t), 128);
+            mbar_init(bar_p(t), 4);                          // one arrival per warp of the half
+            mbar_init(bar_pa(t), 4);
             mbar_init(bar_o(t), 1);
         }
         mbar_init(bar_drain, 1);
@@ -458,8 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             tmem_st32(lane_base + C::q_col(t), qr);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar_q);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_q);
         }
+        // one arrival per warp: every lane's tensor-memory stores are complete
+        // (tcgen05.wait::st + fence by each lane, then the warp converges)
+        auto warp_arrive = [&](uint32_t bar) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar);
+        };
         float m = -INFINITY, l = 0.f;
         int j = 0;
         bool ok = true;
@@ -555,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 if constexpr (C::kHalfP) {
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(bar_pa(t));
+                    warp_arrive(bar_pa(t));
                 }
             } else {
                 uint32_t sr[4][32];
@@ -606,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             if (__any_sync(0xffffffffu, resc) && j > 0) rescale_o(alpha);
                             tmem_wait_st();
                             tc_fence_before();
-                            mbar_arrive(bar_pa(t));
+                            warp_arrive(bar_pa(t));
                         }
                         uint32_t pk[16], pl[16];
 #pragma unroll
@@ -664,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar_p(t));
+            warp_arrive(bar_p(t));
             ++j;
         };
         if constexpr (!kSplit) {
