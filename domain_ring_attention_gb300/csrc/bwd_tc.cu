@@ -60,7 +60,9 @@ struct Cfg {
     static constexpr int kSOff = kOOff + kStages * kTileBytes;     // dS^T (hi), 128 x 128 fp16
     static constexpr int kS2Off = kSOff + 2 * kChunkBytes;         // dS^T lo part (partial tiles)
     static constexpr int kLOff = kS2Off + 2 * kChunkBytes;         // [stage] lse*log2e, Delta
-    static constexpr int kBarOff = kLOff + kStages * 2 * kT * 4;
+    // second dQ staging slice of each softmax warp (the first is its slice of the dS^T lo tile)
+    static constexpr int kDq2Off = kLOff + kStages * 2 * kT * 4;
+    static constexpr int kBarOff = kDq2Off + 8 * 4096;
     // kv_full, q_full[S], q_empty[S], s_full, ds_ready, it_done, dq_free, drain
     static constexpr int kNumBars = 6 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -390,6 +392,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // the lead key tile), so the next pass of an ordinary tile need not
         // wait for the TMA to have read the staged dQ out of it.
         const uint32_t stg = sS2 + (uint32_t)(grp * C::kChunkBytes + quad * 32 * 128);
+        // the warp's second staging slice: successive dQ chunks alternate between
+        // the two, so a chunk waits only for the TMA read of the chunk before the
+        // previous one
+        const uint32_t stg2 = sbase + C::kDq2Off + (uint32_t)((warp - 4) * 4096);
+        int nch = 0;
         // Write (or, after a flush, add) this key row's dV (group 0) or
         // scale * dK (group 1) from the TMEM accumulator into the output.
         auto emit = [&](bool have, bool add) {
@@ -539,11 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             const bool row_ok = quad * 32 + lane < nq;
 #pragma unroll
             for (int c = 0; c < kCols / 32; ++c) {
-                // one staging slice: the TMA has read the previous chunk (or the
-                // previous tile's last chunk) out of it first
-                if (lane == 0) bulk_wait_read_0();
+                // the TMA has read this slice's previous chunk out of it; the other
+                // slice's (most recent) group may still be reading
+                if (lane == 0) bulk_wait_read_1();
                 __syncwarp();
-                const uint32_t buf = stg;
+                const uint32_t buf = (nch++ & 1) ? stg2 : stg;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     // 16-byte unit k of row `lane` under the 128-byte swizzle
