@@ -20,6 +20,14 @@ from ._lib import (  # noqa: F401
     st_halo_exchange,
     st_conv2d_sharded,
     st_group_norm_sharded,
+    st_ring_workspace_size,
+    st_ring_fwd_step,
+    st_ring_bwd_step,
+    st_ring_fwd_local,
+    st_ring_bwd_local,
+    st_attn_bwd_delta,
+    st_convert_f32,
+    st_fp16_scaled_copy,
     ST_DTYPE_BF16,
     ST_DTYPE_F32,
 )

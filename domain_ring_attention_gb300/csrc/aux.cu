@@ -102,31 +102,78 @@ merge_kernel(int nparts, int B, int H, int S, const float* __restrict__ part_out
     }
 }
 
-// Delta_i = sum_c dO_ic * O_ic in fp32 (backward preprocess).
+// N consecutive elements (N = 2 or 4, 4N- or 2N-byte aligned) as floats, one vector load.
+template <int N>
+__device__ __forceinline__ void load_vec(const float* p, float (&x)[N]) {
+    if constexpr (N == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(p);
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else {
+        const float2 v = *reinterpret_cast<const float2*>(p);
+        x[0] = v.x; x[1] = v.y;
+    }
+}
+template <int N>
+__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float (&x)[N]) {
+    if constexpr (N == 4) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+        const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+        x[0] = a.x; x[1] = a.y; x[2] = c.x; x[3] = c.y;
+    } else {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+        x[0] = a.x; x[1] = a.y;
+    }
+}
+
+// Delta_i = sum_c dO_ic * O_ic in fp32 (backward preprocess).  A warp takes 32
+// consecutive positions s of one (b, h): each row is read as one contiguous
+// vector per lane (four rows in flight before any is reduced), lane r keeps
+// the sum of row r, and the 32 sums go out as one coalesced store into
+// Delta[b, h, s0 .. s0+31] (Delta is [B, H, S], the rows [B, S, H]).
 template <typename TO, typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 1)
 delta_kernel(int B, int H, int S, const TO* __restrict__ o, const T* __restrict__ dout,
              float* __restrict__ delta) {
     constexpr int PER = D / 32;
+    constexpr int R = 4;   // rows in flight per warp
     const int lane = threadIdx.x & 31;
-    const int64_t nrows = (int64_t)B * S * H;
-    for (int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); row < nrows;
-         row += (int64_t)gridDim.x * kWarps) {
-        float acc = 0.f;
+    const int sblocks = (S + 31) / 32;
+    const int64_t nunits = (int64_t)B * H * sblocks;
+    for (int64_t u = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < nunits;
+         u += (int64_t)gridDim.x * kWarps) {
+        const int sb = (int)(u % sblocks);
+        const int64_t bh = u / sblocks;
+        const int h = (int)(bh % H);
+        const int b = (int)(bh / H);
+        const int s0 = sb * 32;
+        float mine = 0.f;
+#pragma unroll 1
+        for (int r0 = 0; r0 < 32; r0 += R) {
+            float vo[R][PER], vg[R][PER];
 #pragma unroll
-        for (int e = 0; e < PER; ++e) {
-            const int64_t i = row * D + lane * PER + e;
-            acc = fmaf(to_f32(o[i]), to_f32(dout[i]), acc);
-        }
+            for (int r = 0; r < R; ++r) {
+                const int s = s0 + r0 + r;
+                if (s < S) {
+                    const int64_t row = ((int64_t)b * S + s) * H + h;
+                    load_vec<PER>(o + row * D + lane * PER, vo[r]);
+                    load_vec<PER>(dout + row * D + lane * PER, vg[r]);
+                }
+            }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
-            const int h = (int)(row % H);
-            const int64_t bs = row / H;
-            const int s = (int)(bs % S);
-            const int b = (int)(bs / S);
-            delta[((int64_t)b * H + h) * S + s] = acc;
+            for (int r = 0; r < R; ++r) {
+                float acc = 0.f;
+                if (s0 + r0 + r < S) {
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) acc = fmaf(vo[r][e], vg[r][e], acc);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                if (lane == r0 + r) mine = acc;
+            }
         }
+        if (s0 + lane < S) delta[bh * S + s0 + lane] = mine;
     }
 }
 
