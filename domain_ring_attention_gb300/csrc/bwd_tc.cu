@@ -58,7 +58,7 @@ struct Cfg {
     static constexpr int kQOff = kVOff + kTileBytes;               // [stage] Q tiles
     static constexpr int kOOff = kQOff + kStages * kTileBytes;     // [stage] dO tiles
     static constexpr int kSOff = kOOff + kStages * kTileBytes;     // dS^T (hi), 128 x 128 fp16
-    static constexpr int kS2Off = kSOff + 2 * kChunkBytes;         // dS^T lo part (partial tiles)
+    static constexpr int kS2Off = kSOff + 2 * kChunkBytes;         // dS^T lo part (split tiles)
     static constexpr int kLOff = kS2Off + 2 * kChunkBytes;         // [stage] lse*log2e, Delta
     // second dQ staging slice of each softmax warp (the first is its slice of the dS^T lo tile)
     static constexpr int kDq2Off = kLOff + kStages * 2 * kT * 4;
@@ -182,12 +182,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
     const int tile = p.use_order ? (int)p.order[blockIdx.x] : (int)blockIdx.x;
     const QTile kt = locate_qtile(p.tab, tile, kT);           // this CTA's key tile
     // Extra precision (hi + lo fp16 parts of P and dS) where gradients are
-    // large compared with their RMS: partial (diagonal / ragged) tiles, which
+    // large compared with their RMS: tiles on the causal diagonal, which
     // hold the rows and keys with few partners, and under causal masking the
     // key tile holding the first natural positions, which every query attends
     // to (its dV and dK are orders of magnitude above the typical key's).
     const bool lead_tile = p.causal && kt.nat0 < kT;
-    auto wants_split = [&](int kind) { return kind == kPartial || lead_tile; };
+    auto wants_split = [&](int kind, int natq) {
+        return (kind == kPartial && on_diagonal(p.causal, natq, kt.nat0, kt.nq)) || lead_tile;
+    };
     // fp32 gradients of the lead key tile: its dV and dK sum tens of thousands
     // of products, and the tensor core's fp32 accumulation of that many terms
     // drifts by ~1e-4 relative -- on the largest gradients of the tensor.  So
@@ -332,12 +334,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 ok = mbar_wait(bar_ds, i & 1, abort_flag);
                 if (!ok) return;
                 tc_fence_after();
-                // Partial (diagonal / ragged) tiles hold the pairs of rows and
-                // keys with few partners, whose P and dS are large: there both
+                // Tiles on the causal diagonal hold the pairs of rows and keys
+                // with few partners, whose P and dS are large: there (and on
+                // the lead key tile) both
                 // are split into fp16 hi + lo parts (P_lo in the consumed dP^T
                 // columns, dS_lo in a second smem tile) and every product gets
                 // a second MMA for the lo part.
-                const bool split = wants_split(classify(causal, natq, nq, kt.nat0, kt.nq, kT));
+                const bool split = wants_split(classify(causal, natq, nq, kt.nat0, kt.nq, kT), natq);
                 // dV += P^T dO  (A: P^T fp16 in TMEM; B: dO, K = query rows, N = D)
 #pragma unroll
                 for (int kk = 0; kk < kT / 16; ++kk)
@@ -388,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         const float sc = ldexpf(p.scale, p.exps[4] + p.exps[1]);           // dQ_t -> dQ
         // dQ staging: the 4 KB of the dS^T lo tile that this warp itself
         // writes -- its 32 key rows of its group's 64 columns.  The lo tile is
-        // written only by the softmax passes of split tiles (partial tiles and
+        // written only by the softmax passes of split tiles (the causal diagonal and
         // the lead key tile), so the next pass of an ordinary tile need not
         // wait for the TMA to have read the staged dQ out of it.
         const uint32_t stg = sS2 + (uint32_t)(grp * C::kChunkBytes + quad * 32 * 128);
@@ -591,14 +594,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             const int kind = classify(causal, natq, nq, kt.nat0, kt.nq, kT);
             // a pass that writes the lo tile waits until the TMA has read the
             // dQ staged in this warp's slice of it
-            if (kind == kPartial || lead_tile) {
+            const bool lo = wants_split(kind, natq);
+            if (lo) {
                 if (lane == 0) bulk_wait_read_0();
                 __syncwarp();
             }
             if (kind == kPartial) {
                 // causal: query column c sees key natk iff natk <= natq + c
                 const int cmin = causal ? max(0, natk - natq) : 0;
-                tile_pass(std::true_type{}, std::true_type{}, ls, cmin);
+                if (lo)
+                    tile_pass(std::true_type{}, std::true_type{}, ls, cmin);
+                else
+                    tile_pass(std::true_type{}, std::false_type{}, ls, cmin);
             } else if (lead_tile) {
                 tile_pass(std::false_type{}, std::true_type{}, ls, 0);
             } else {

@@ -37,6 +37,14 @@ __device__ __forceinline__ QTile locate_qtile(const SegTable& T, int tile, int t
 // Classification of a (query tile, KV tile) pair.
 enum TileKind { kSkip = 0, kFull = 1, kPartial = 2 };
 
+// A partial pair on the causal diagonal: some of its keys come after the first
+// query.  Its rows and keys have few partners, so P and dS there get the extra
+// hi / lo precision; a pair that is partial only because its KV tile is ragged
+// needs the key mask alone.
+__device__ __forceinline__ bool on_diagonal(int causal, int nat_q0, int nat_k0, int nk) {
+    return causal && nat_k0 + nk - 1 > nat_q0;
+}
+
 __device__ __forceinline__ int classify(int causal, int nat_q0, int nq, int nat_k0, int nk,
                                         int tile_cols) {
     if (causal && nat_k0 > nat_q0 + nq - 1) return kSkip;

@@ -162,8 +162,9 @@ __device__ __forceinline__ int half_kind(int causal, int nat0, int nq, int natk,
     return classify(causal, nat0, nq, natk, nk, kN);
 }
 
-// kSplit: compiled with the hi/lo path for partial tiles (causal masks or
-// ragged shards); layouts whose tiles are all full use the kernel without it.
+// kSplit: compiled with the mask and the hi/lo path for partial tiles (causal
+// masks or ragged shards; the hi/lo split itself only on the causal diagonal);
+// layouts whose tiles are all full use the kernel without either.
 // kMode: what the kernel writes.
 //   kFused    out, lse of the whole ring (the running state carried across KV shards)
 //   kParts    the partials mode -- instead of carrying the running state from one
@@ -335,10 +336,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             // PV_t in two halves of 64 keys (part 0: keys 0-63, issued as soon
             // as the softmax has written P for them; part 1 once all of P_t is
             // in), so that fewer MMAs stand between a finished softmax pass and
-            // the next S_t.  Partial (diagonal / ragged) tiles carry the rows
-            // with few visible keys, whose P entries are large: there P = P_hi
-            // + P_lo (both fp16, P_lo in the upper 64 columns of the S region)
-            // and a second MMA adds P_lo V.
+            // the next S_t.  Tiles on the causal diagonal carry the rows with
+            // few visible keys, whose P entries are large: there P = P_hi +
+            // P_lo (both fp16, P_lo in the upper 64 columns of the S region)
+            // and a second MMA adds P_lo V.  A tile that is partial only
+            // because its shard ends inside it needs the key mask alone: its
+            // rows see every key of the other tiles as well.
             // (part 0: keys 0-63, part 1: keys 64-127, part -1: all keys)
             // `fresh`: O_t starts from zero with this tile (the first tile
             // overall; in the partials mode the first tile of every KV shard)
@@ -412,8 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 int prev_shard = -1;
                 ring_walk<kN>(p.kvtab, qt.shard, [&](int js, int, int nk, int natk, bool) {
                     if (!ok || !active(nk, natk)) return;
-                    step(half_kind(causal, nat_h[0], nq_h[0], natk, nk) == kPartial,
-                         half_kind(causal, nat_h[1], nq_h[1], natk, nk) == kPartial, js != prev_shard);
+                    step(half_kind(causal, nat_h[0], nq_h[0], natk, nk) == kPartial &&
+                             on_diagonal(causal, nat_h[0], natk, nk),
+                         half_kind(causal, nat_h[1], nq_h[1], natk, nk) == kPartial &&
+                             on_diagonal(causal, nat_h[1], natk, nk),
+                         js != prev_shard);
                     prev_shard = js;
                 });
             }
@@ -601,8 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
                 uint64_t acc0 = 0, acc1 = 0;   // two packed partial sums (0.0f bits)
                 // Two compile-time variants of the exponential pass, so the full
-                // tiles run without the split code: partial tiles write
-                // P = P_hi + P_lo, both fp16 (see issue_pv).
+                // tiles run without the split code: tiles on the causal
+                // diagonal write P = P_hi + P_lo, both fp16 (see issue_pv).
                 auto exp_pass = [&](auto split_tag) {
                     constexpr bool kLo = decltype(split_tag)::value;
 #pragma unroll
@@ -634,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         tmem_st16(tS + c * 16, pk);
                         if constexpr (kLo) {
                             // second pass over the chunk for the lo parts: the
-                            // exponentials are recomputed (partial tiles only)
+                            // exponentials are recomputed (diagonal tiles only)
                             // rather than kept alive next to the hi parts
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
@@ -651,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     }
                 };
                 if constexpr (kSplit) {
-                    if (kind == kPartial)
+                    if (kind == kPartial && on_diagonal(causal, nat_h[t], natk, nk))
                         exp_pass(std::true_type{});
                     else
                         exp_pass(std::false_type{});
