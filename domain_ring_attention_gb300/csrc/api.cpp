@@ -299,6 +299,103 @@ extern "C" int st_attn_fwd(const st_layout_t* L, int B, int H, int d, int dtype,
     return cuda_status(st::launch_fwd_simt(t, a, dtype, stream));
 }
 
+namespace {
+
+// st_attn_fwd_host with the heads in groups: per group, the 2-D copies of its
+// heads' V, K and Q (pitch H * d), the exact fp16 copy of its V with an
+// exponent of its own, the attention launch over its heads, and its output
+// and lse copied back.  Groups alternate between `stream` and a second stream
+// made here, so that one group's last wave overlaps the next group's first.
+int fwd_host_groups(const st_layout_t* L, const st::SegTable& t, int B, int H, int d, int causal, float scale,
+                    int hn_mid, const void* q_host, const void* k_host, const void* v_host, void* out_host,
+                    float* lse_host, void* q, void* k, void* v, void* out, float* lse, void* workspace,
+                    size_t need, void* stream, void* copy_stream) {
+    // group boundaries: a single head first and last (little to copy in before
+    // the first launch, little to copy back after the last), hn_mid between
+    std::vector<int> hb{0};
+    if (H >= 3) hb.push_back(1);
+    while (hb.back() < H - 1) hb.push_back(std::min(H - 1, hb.back() + hn_mid));
+    if (hb.back() < H) hb.push_back(H);
+    const int G = (int)hb.size() - 1;
+    const int64_t S = L->S;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
+    cudaStream_t s2 = nullptr;
+    // ev[0]: work queued on `stream` before this call, later the last copy
+    // back; per group g: V landed (1 + 3g), K and Q landed (2 + 3g), computed (3 + 3g)
+    std::vector<cudaEvent_t> ev(1 + 3 * G, nullptr);
+    int rc = ST_OK;
+    auto ck = [&](cudaError_t e) { return cuda_status((int)e); };
+    auto finish = [&](int code) {
+        for (auto& e : ev)
+            if (e) cudaEventDestroy(e);   // released once pending work has passed it
+        if (s2) cudaStreamDestroy(s2);    // likewise: its queued work still runs
+        return code;
+    };
+    for (auto& e : ev)
+        if ((rc = ck(cudaEventCreateWithFlags(&e, cudaEventDisableTiming))) != ST_OK) return finish(rc);
+    if ((rc = ck(cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking))) != ST_OK) return finish(rc);
+    const size_t pitch = (size_t)H * d * 2;        // one token of q, k, v or out (bf16)
+    const size_t hw = (size_t)d * 2;               // one head within it
+    const size_t rows = (size_t)B * S;
+    // everything queued on `stream` before this call comes first on all three streams
+    if ((rc = ck(cudaEventRecord(ev[0], cs))) != ST_OK) return finish(rc);
+    if ((rc = ck(cudaStreamWaitEvent(xs, ev[0], 0))) != ST_OK) return finish(rc);
+    if ((rc = ck(cudaStreamWaitEvent(s2, ev[0], 0))) != ST_OK) return finish(rc);
+    for (int g = 0; g < G; ++g) {
+        const size_t off = (size_t)hb[g] * hw, gw = (size_t)(hb[g + 1] - hb[g]) * hw;
+        auto h2d = [&](void* dst, const void* src) {
+            return ck(cudaMemcpy2DAsync(static_cast<char*>(dst) + off, pitch, static_cast<const char*>(src) + off,
+                                        pitch, gw, rows, cudaMemcpyHostToDevice, xs));
+        };
+        if ((rc = h2d(v, v_host)) != ST_OK) return finish(rc);
+        if ((rc = ck(cudaEventRecord(ev[1 + 3 * g], xs))) != ST_OK) return finish(rc);
+        if ((rc = h2d(k, k_host)) != ST_OK) return finish(rc);
+        if ((rc = h2d(q, q_host)) != ST_OK) return finish(rc);
+        if ((rc = ck(cudaEventRecord(ev[2 + 3 * g], xs))) != ST_OK) return finish(rc);
+    }
+    char* ws = static_cast<char*>(workspace);
+    unsigned* amax = reinterpret_cast<unsigned*>(ws + need - 256);   // one per group (G <= 18 < 32)
+    int* exps = reinterpret_cast<int*>(ws + need - 128);
+    for (int g = 0; g < G; ++g) {
+        cudaStream_t gs = (g & 1) ? s2 : cs;
+        const int hn = hb[g + 1] - hb[g];
+        const size_t off = (size_t)hb[g] * hw, gw = (size_t)hn * hw;
+        if ((rc = ck(cudaStreamWaitEvent(gs, ev[1 + 3 * g], 0))) != ST_OK) return finish(rc);
+        // the fp16 copy of V lives at the same offsets as V (2 bytes per element)
+        if ((rc = cuda_status(st::launch_fp16_copy_rows(static_cast<char*>(v) + off, ws + off, (int64_t)rows,
+                                                        (int)(gw / 16), (int64_t)(pitch / 16), amax + g, exps + g,
+                                                        gs))) != ST_OK)
+            return finish(rc);
+        if ((rc = ck(cudaStreamWaitEvent(gs, ev[2 + 3 * g], 0))) != ST_OK) return finish(rc);
+        st::AttnArgs a{q, k, v, out, lse, nullptr, nullptr, B, H, d, causal ? 1 : 0, scale, ST_DTYPE_BF16,
+                       ws, amax + g, exps + g};
+        a.h0 = hb[g];
+        a.hn = hn;
+        bool handled = false;
+        rc = st::launch_fwd_tc(*L, a, gs, &handled, 0, t.ntiles);
+        if (!handled) return finish(ST_ERR_UNSUPPORTED);
+        if ((rc = cuda_status(rc)) != ST_OK) return finish(rc);
+        if ((rc = ck(cudaEventRecord(ev[3 + 3 * g], gs))) != ST_OK) return finish(rc);
+        // this group's output and lse back to the host while the next group runs
+        if ((rc = ck(cudaStreamWaitEvent(xs, ev[3 + 3 * g], 0))) != ST_OK) return finish(rc);
+        if ((rc = ck(cudaMemcpy2DAsync(static_cast<char*>(out_host) + off, pitch, static_cast<const char*>(out) + off,
+                                       pitch, gw, rows, cudaMemcpyDeviceToHost, xs))) != ST_OK)
+            return finish(rc);
+        // lse [B, H, S]: the group's hn * S values of every batch entry
+        const size_t lo = (size_t)hb[g] * S;
+        if ((rc = ck(cudaMemcpy2DAsync(lse_host + lo, (size_t)H * S * 4, lse + lo, (size_t)H * S * 4,
+                                       (size_t)hn * S * 4, (size_t)B, cudaMemcpyDeviceToHost, xs))) != ST_OK)
+            return finish(rc);
+    }
+    // `stream` completes only after the last copy back (which follows every group)
+    if ((rc = ck(cudaEventRecord(ev[0], xs))) != ST_OK) return finish(rc);
+    if ((rc = ck(cudaStreamWaitEvent(cs, ev[0], 0))) != ST_OK) return finish(rc);
+    return finish(ST_OK);
+}
+
+}  // namespace
+
 extern "C" int st_attn_fwd_host(const st_layout_t* L, int B, int H, int d, int dtype, int causal, float scale,
                                 const void* q_host, const void* k_host, const void* v_host, void* out_host,
                                 float* lse_host, void* q, void* k, void* v, void* out, float* lse,
@@ -329,13 +426,28 @@ extern "C" int st_attn_fwd_host(const st_layout_t* L, int B, int H, int d, int d
         while (t.seg_tile[sgm + 1] <= tl) ++sgm;
         return t.seg_buf[sgm] + (int64_t)(tl - t.seg_tile[sgm]) * tile_rows;
     };
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // Heads in groups, when groups of hn heads still make launches of at least
+    // four waves of CTAs (a single head first and last, hn between): every query
+    // tile needs all of its head's K and V, so with groups only the first
+    // group's K, V (and Q) stand before the first launch, the rest arriving
+    // while earlier groups compute, and only the last group's output is copied
+    // back after the compute.
+    int hn = H;
+    for (int g = 2; g <= std::min(H, 16); ++g) {
+        if (H % g) continue;
+        if ((int64_t)t.ntiles * B * (H / g) < 4LL * std::max(sms, 1)) break;
+        hn = H / g;
+    }
+    if (hn < H)
+        return fwd_host_groups(L, t, B, H, d, causal, scale, hn, q_host, k_host, v_host, out_host, lse_host, q, k,
+                               v, out, lse, workspace, need, stream, copy_stream);
     // Chunks of query tiles: a short first chunk (about two waves of CTAs) so
     // that compute starts early while the rest of Q arrives, a short last
     // chunk so that little output is left to copy back after compute ends, and
     // the bulk in between (whole waves where possible).
-    int sms = 0, dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int per_tile = B * H;                          // CTAs per query tile
     const int edge = std::max(1, (2 * std::max(sms, 1) + per_tile - 1) / per_tile);
     std::vector<int> cuts{0};

@@ -351,6 +351,57 @@ fp16_copy_kernel(int64_t n8, int ds_d, const __grid_constant__ Fp16Job job,
     }
 }
 
+// max |x| over nrows strided rows of row8 8-element units (bf16), one warp per row
+__global__ void __launch_bounds__(256)
+amax_rows_kernel(int64_t nrows, int row8, int64_t pitch8, const uint4* __restrict__ src,
+                 unsigned* __restrict__ amax_bits) {
+    const int lane = threadIdx.x & 31;
+    float m = 0.f;
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < nrows;
+         r += (int64_t)gridDim.x * (blockDim.x >> 5)) {
+        const uint4* row = src + r * pitch8;
+        for (int c = lane; c < row8; c += 32) {
+            const uint4 x = row[c];
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+                m = fmaxf(m, fmaxf(fabsf(__bfloat162float(v2.x)), fabsf(__bfloat162float(v2.y))));
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) atomicMax(amax_bits, __float_as_uint(m));
+}
+
+// dst = src * 2^-e over the same strided rows (exact fp16), e -> exps[0]
+__global__ void __launch_bounds__(256)
+fp16_copy_rows_kernel(int64_t nrows, int row8, int64_t pitch8, const uint4* __restrict__ src,
+                      uint4* __restrict__ dst, const unsigned* __restrict__ amax_bits, int* __restrict__ exps) {
+    const int e = norm_exp(__uint_as_float(amax_bits[0]), 13);
+    const float mul = ldexpf(1.f, -e);
+    if (blockIdx.x == 0 && threadIdx.x == 0) exps[0] = e;
+    const int lane = threadIdx.x & 31;
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < nrows;
+         r += (int64_t)gridDim.x * (blockDim.x >> 5)) {
+        const uint4* srow = src + r * pitch8;
+        uint4* drow = dst + r * pitch8;
+        for (int c = lane; c < row8; c += 32) {
+            const uint4 x = srow[c];
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w[q]);
+                __half2 h2 = __floats2half2_rn(__bfloat162float(v2.x) * mul, __bfloat162float(v2.y) * mul);
+                o[q] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            drow[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
 int fp16_grid(int64_t n8) {
     static int sms = 0;
     if (sms == 0) {
@@ -396,6 +447,18 @@ int launch_fp16_copy1(const void* src, void* dst, int64_t elems, unsigned* amax_
     if (e != cudaSuccess) return (int)e;
     amax_kernel<1><<<grid, 256, 0, st>>>(n8, job, amax_bits);
     fp16_copy_kernel<1><<<grid, 256, 0, st>>>(n8, 0, job, amax_bits, exps);
+    return (int)cudaGetLastError();
+}
+
+int launch_fp16_copy_rows(const void* src, void* dst, int64_t nrows, int row8, int64_t pitch8,
+                          unsigned* amax_bits, int* exps, void* stream) {
+    const int grid = fp16_grid(nrows * 32);    // 8 rows (warps) per 256-thread block
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(amax_bits, 0, sizeof(unsigned), st);
+    if (e != cudaSuccess) return (int)e;
+    amax_rows_kernel<<<grid, 256, 0, st>>>(nrows, row8, pitch8, static_cast<const uint4*>(src), amax_bits);
+    fp16_copy_rows_kernel<<<grid, 256, 0, st>>>(nrows, row8, pitch8, static_cast<const uint4*>(src),
+                                                static_cast<uint4*>(dst), amax_bits, exps);
     return (int)cudaGetLastError();
 }
 

@@ -66,6 +66,9 @@ struct AttnArgs {
     // call's partial is merged into by the log-sum-exp rule, or nullptr
     const float* prev_out;
     const float* prev_lse;
+    // heads h0 .. h0 + hn - 1 only (hn = 0: all heads); the tensors keep all H
+    int h0 = 0;
+    int hn = 0;
 };
 
 // Workspace of st_attn_fwd: bf16 needs the fp16 copy of v plus 256 bytes.
@@ -154,6 +157,11 @@ int launch_fp16_copies(const BwdArgs& a, int64_t S, void* stream, int64_t Skv = 
 // One bf16 tensor -> exact fp16 copy scaled by 2^-exps[0] (forward: V)
 int launch_fp16_copy1(const void* src, void* dst, int64_t elems, unsigned* amax_bits, int* exps,
                       void* stream);
+// The same over a strided set of rows: nrows rows of row8 8-element units each,
+// pitch8 units apart (the heads of one group of a [B,S,H,d] tensor); the
+// scale and exponent cover these rows only.
+int launch_fp16_copy_rows(const void* src, void* dst, int64_t nrows, int row8, int64_t pitch8,
+                          unsigned* amax_bits, int* exps, void* stream);
 int launch_dq_convert(const BwdArgs& a, int64_t S, int dtype, void* stream);
 int launch_permute(const SegTable& t, int B, int H, int d, int dtype, int to_natural,
                    const void* in, void* out, void* stream);

@@ -110,6 +110,7 @@ struct FwdParams {
     void* out;                 // bf16, or fp32 when out_f32
     float* lse;
     int B, H;
+    int h0, hn;                // this launch's heads: h0 .. h0 + hn - 1 (grid y = B * hn)
     float scale_log2;          // softmax scale * log2(e)
     int causal;
     int out_f32;
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = p.H;
-    const int b = blockIdx.y / H, h = blockIdx.y % H;
+    const int b = blockIdx.y / p.hn, h = p.h0 + (int)(blockIdx.y % p.hn);
     const int tile = p.use_order ? (int)p.order[blockIdx.x] : p.tile0 + (int)blockIdx.x;
     const QTile qt = locate_qtile(p.tab, tile, kNQ * kM);
     int nq_h[kNQ], nat_h[kNQ];
@@ -861,12 +862,14 @@ int launch_t(const st_layout& L, const st_layout& Lkv, const AttnArgs& a, void* 
     p.prev_lse = a.prev_lse;
     p.B = a.B;
     p.H = a.H;
+    p.h0 = a.hn > 0 ? a.h0 : 0;
+    p.hn = a.hn > 0 ? a.hn : a.H;
     p.scale_log2 = a.scale * kLog2e;
     p.causal = a.causal;
     auto kern = fwd_tc_kernel<D, kSplit, kMode>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return (int)e;
-    dim3 grid(t1 - t0, a.B * a.H);
+    dim3 grid(t1 - t0, a.B * p.hn);
     kern<<<grid, kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
     return (int)cudaGetLastError();
 }

@@ -135,16 +135,29 @@ int st_attn_fwd(const st_layout_t* layout, int B, int H, int d, int dtype, int c
  *   copy_stream            : a second stream, distinct from `stream`, that
  *                            carries the copies.
  * Order of work (stream-ordered: nothing starts before the work already
- * queued on `stream` at the call, which copy_stream is made to wait for):
- *   1. V, then K, are copied in on copy_stream; every query tile needs all of
- *      them.  The fp16 copy of V runs on `stream` while K arrives.
- *   2. Q follows on copy_stream in three chunks of query tiles: a short first
- *      chunk (about two waves of CTAs), the bulk, and a short last chunk.
- *   3. Each chunk is computed on `stream` as soon as its rows have arrived.
- *   4. Its output rows and lse go back on copy_stream while the next chunk
- *      computes.
+ * queued on `stream` at the call, which the other streams are made to wait
+ * for).  Every query tile needs all of its head's K and V, so the work is
+ * split by heads where it can be:
+ *   - Head groups, when H has a divisor G (2 <= G <= 16) whose groups of
+ *     hn = H / G heads still launch at least four waves of CTAs (the largest
+ *     such G): a single head first and last, groups of up to hn heads between.
+ *     Per group, V, K and Q of its heads are copied in on copy_stream (2-D
+ *     copies, pitch H * d); the fp16 copy of its V (with a scale of its own)
+ *     and its attention launch run once they have landed, on `stream` and on
+ *     a second stream made for the call, alternately, so that one group's
+ *     last wave overlaps the next group's first; its output and lse go back
+ *     on copy_stream while the next group computes.  Only the first group's
+ *     inputs stand before the first launch, and only the last group's outputs
+ *     are copied back after the last.
+ *   - Otherwise: V, then K, are copied in whole on copy_stream (the fp16 copy
+ *     of V runs on `stream` while K arrives); Q follows in three chunks of
+ *     query tiles (a short first chunk of about two waves of CTAs, the bulk,
+ *     a short last chunk); each chunk is computed on `stream` once its rows
+ *     have arrived, and its output rows and lse go back on copy_stream while
+ *     the next chunk computes.
  * When `stream` has completed, every output is in host memory.  A few CUDA
- * events are created and released per call; no device memory is allocated.
+ * events (and, with head groups, one stream) are created and released per
+ * call; no device memory is allocated.
  * Errors: as st_attn_fwd, plus ST_ERR_UNSUPPORTED for dtype other than bf16
  * and ST_ERR_INVALID_ARG when copy_stream is NULL or equal to stream. */
 int st_attn_fwd_host(const st_layout_t* layout, int B, int H, int d, int dtype, int causal, float scale,

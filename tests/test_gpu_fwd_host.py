@@ -1,10 +1,14 @@
 """GPU checks of the host-buffer forward (st_attn_fwd_host).
 
 It must give, bit for bit, what st_attn_fwd gives on the same inputs: the same kernels on the same tiles, only
-launched per chunk of query tiles with the copies overlapped. The cases:
-- one chunk (few tiles);
-- three chunks (B * H = 64 CTAs per query tile);
-- causal zigzag over uneven shards, where the tile order inside each chunk is heaviest first.
+launched per group of heads (or per chunk of query tiles) with the copies overlapped.  With head groups the fp16
+copy of V is scaled per group, by another power of two than the whole tensor's; the products and the final
+normalisation then differ by exact powers of two only, so the outputs are still the same bits.  The cases:
+- one chunk (few tiles, H = 4: no head groups);
+- head groups of 1, 16, 14 and 1 heads (B * H * tiles large enough for groups of 16);
+- head groups of 1, 4, 4, 4, 2 and 1 heads;
+- causal zigzag over uneven shards in head groups of 1, 16, 14 and 1 (heaviest tiles first within each group);
+- three chunks of query tiles (H = 3 has no divisor that leaves four waves per group).
 A few rows are also held to the oracle with the bf16 bounds.
 """
 import numpy as np
@@ -21,8 +25,10 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("B,H,d,lens,causal,zigzag", [
     (1, 4, 64, (512,) * 8, False, False),              # one chunk
-    (2, 32, 64, (1024,) * 8, False, False),            # three chunks: 5 + 22 + 5 tiles
-    (2, 32, 128, (2560, 1536, 3328, 768), True, True),  # three chunks, causal zigzag, uneven shards
+    (2, 32, 64, (1024,) * 8, False, False),            # head groups of 1, 16, 14, 1
+    (2, 16, 64, (2432,) * 8, False, False),            # head groups of 1, 4, 4, 4, 2, 1 (80 tiles x 2 CTAs per head)
+    (2, 32, 128, (2560, 1536, 3328, 768), True, True),  # head groups of 1, 16, 14, 1; causal zigzag, uneven shards
+    (2, 3, 64, (8192,) * 8, False, False),             # three chunks of query tiles: 51 + 154 + 51
 ])
 def test_host_forward_equals_device_forward(B, H, d, lens, causal, zigzag):
     wl = Workload("host", B=B, H=H, d=d, lens=lens, causal=causal, zigzag=zigzag, dtype="bf16")
