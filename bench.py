@@ -639,8 +639,8 @@ def run_ours(args, rank, world):
 
         def e2e_step():
             if out.dtype == torch.bfloat16:
-                # the host-buffer entry point: V and K in first, Q in chunks, each
-                # chunk's output copied back while the next one computes
+                # the host-buffer entry point: heads in groups, each group's copies
+                # in, compute and copies back overlapped with the other groups'
                 st.st_attn_fwd_host(lay, pin[0], pin[1], pin[2], out_h, lse_h, dev, causal=wl.causal,
                                     workspace=ws, stream=stream, copy_stream=copy_stream)
                 return
