@@ -110,7 +110,6 @@ struct FwdParams {
     void* out;                 // bf16, or fp32 when out_f32
     float* lse;
     int B, H;
-    int h0, hn;                // this launch's heads: h0 .. h0 + hn - 1 (grid y = B * hn)
     float scale_log2;          // softmax scale * log2(e)
     int causal;
     int out_f32;
@@ -125,6 +124,13 @@ struct FwdParams {
     int use_order;             // causal: CTAs take tiles heaviest first
     int tile0;                 // first query tile of this launch (without an order)
     uint16_t order[kMaxOrder];
+};
+
+// The parameters of a launch over the heads h0 .. h0 + hn - 1 only (grid y = B * hn):
+// the host-buffer forward computes the heads in groups.  A type of its own, so
+// that the ordinary launches keep their parameter block as it is.
+struct FwdParamsHeads : FwdParams {
+    int h0, hn;
 };
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -177,8 +183,12 @@ __device__ __forceinline__ int half_kind(int causal, int nat0, int nq, int natk,
 //             rule into the running state prev_out, prev_lse.  Compiled with kSplit.
 enum { kFused = 0, kParts = 1, kMerge = 2 };
 
-template <int D, bool kSplit, int kMode>
-__global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p) {
+// kHeads: the launch covers the heads h0 .. h0 + hn - 1 only (FwdParamsHeads);
+// a separate instantiation, so that the ordinary launches keep the plain (b, h)
+// decoding.
+template <int D, bool kSplit, int kMode, bool kHeads>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ std::conditional_t<kHeads, FwdParamsHeads, FwdParams> p) {
     static_assert(kSplit || kMode == kFused, "partials and ring steps walk the ring with the split kernel");
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -204,7 +214,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = p.H;
-    const int b = blockIdx.y / p.hn, h = p.h0 + (int)(blockIdx.y % p.hn);
+    int b, h;
+    if constexpr (kHeads) {
+        b = blockIdx.y / p.hn;
+        h = p.h0 + blockIdx.y % p.hn;
+    } else {
+        b = blockIdx.y / H;
+        h = blockIdx.y % H;
+    }
     const int tile = p.use_order ? (int)p.order[blockIdx.x] : p.tile0 + (int)blockIdx.x;
     const QTile qt = locate_qtile(p.tab, tile, kNQ * kM);
     int nq_h[kNQ], nat_h[kNQ];
@@ -816,10 +833,10 @@ bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int d,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool kSplit, int kMode>
+template <int D, bool kSplit, int kMode, bool kHeads = false>
 int launch_t(const st_layout& L, const st_layout& Lkv, const AttnArgs& a, void* stream, int t0, int t1) {
     using C = Cfg<D>;
-    FwdParams p;
+    std::conditional_t<kHeads, FwdParamsHeads, FwdParams> p;
     const int S = (int)L.S, Skv = (int)Lkv.S;
     if (!make_map(&p.tq, a.q, a.B, S, a.H, D) || !make_map(&p.tk, a.k, a.B, Skv, a.H, D) ||
         !make_map(&p.tv, a.v16, a.B, Skv, a.H, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
@@ -862,14 +879,17 @@ int launch_t(const st_layout& L, const st_layout& Lkv, const AttnArgs& a, void* 
     p.prev_lse = a.prev_lse;
     p.B = a.B;
     p.H = a.H;
-    p.h0 = a.hn > 0 ? a.h0 : 0;
-    p.hn = a.hn > 0 ? a.hn : a.H;
+    int hn = a.H;
+    if constexpr (kHeads) {
+        p.h0 = a.h0;
+        p.hn = hn = a.hn;
+    }
     p.scale_log2 = a.scale * kLog2e;
     p.causal = a.causal;
-    auto kern = fwd_tc_kernel<D, kSplit, kMode>;
+    auto kern = fwd_tc_kernel<D, kSplit, kMode, kHeads>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return (int)e;
-    dim3 grid(t1 - t0, a.B * p.hn);
+    dim3 grid(t1 - t0, a.B * hn);
     kern<<<grid, kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
     return (int)cudaGetLastError();
 }
@@ -884,6 +904,16 @@ int launch_fwd_tc2(const st_layout& L, const st_layout& Lkv, const AttnArgs& a, 
     bool split = a.causal != 0;
     for (size_t s = 0; s + 1 < Lkv.seg_buf.size(); ++s)
         split |= ((Lkv.seg_buf[s + 1] - Lkv.seg_buf[s]) % kN) != 0;
+    // a head range (h0, hn): the fused forward of the host-buffer entry point only
+    const bool heads = a.hn > 0 && a.hn < a.H;
+    if (heads && (a.part_out || a.prev_out || a.h0 < 0 || a.h0 + a.hn > a.H)) return (int)cudaErrorInvalidValue;
+    if (heads) {
+        if (a.d == 64)
+            return split ? launch_t<64, true, kFused, true>(L, Lkv, a, stream, t0, t1)
+                         : launch_t<64, false, kFused, true>(L, Lkv, a, stream, t0, t1);
+        return split ? launch_t<128, true, kFused, true>(L, Lkv, a, stream, t0, t1)
+                     : launch_t<128, false, kFused, true>(L, Lkv, a, stream, t0, t1);
+    }
     if (a.part_out) {
         // partials: the ring walk of the split kernel, state written per KV shard
         return a.d == 64 ? launch_t<64, true, kParts>(L, Lkv, a, stream, t0, t1)
