@@ -8,7 +8,9 @@ normalisation then differ by exact powers of two only, so the outputs are still 
 - head groups of 1, 16, 14 and 1 heads (B * H * tiles large enough for groups of 16);
 - head groups of 1, 4, 4, 4, 2 and 1 heads;
 - causal zigzag over uneven shards in head groups of 1, 16, 14 and 1 (heaviest tiles first within each group);
-- three chunks of query tiles (H = 3 has no divisor that leaves four waves per group).
+- three chunks of query tiles (H = 3 has no divisor that leaves four waves per group);
+- head groups of uneven sizes (1, 3, 1, 1 for H = 6);
+- causal zigzag at d = 64 in head groups of 1, 2, 2, 2, 1.
 A few rows are also held to the oracle with the bf16 bounds.
 """
 import numpy as np
@@ -29,6 +31,8 @@ pytestmark = pytest.mark.gpu
     (2, 16, 64, (2432,) * 8, False, False),            # head groups of 1, 4, 4, 4, 2, 1 (80 tiles x 2 CTAs per head)
     (2, 32, 128, (2560, 1536, 3328, 768), True, True),  # head groups of 1, 16, 14, 1; causal zigzag, uneven shards
     (2, 3, 64, (8192,) * 8, False, False),             # three chunks of query tiles: 51 + 154 + 51
+    (1, 6, 64, (16384,) * 4, False, False),            # head groups of 1, 3, 1, 1
+    (2, 8, 64, (12288, 20480, 4096, 2048), True, True),  # head groups of 1, 2, 2, 2, 1; causal zigzag, d = 64
 ])
 def test_host_forward_equals_device_forward(B, H, d, lens, causal, zigzag):
     wl = Workload("host", B=B, H=H, d=d, lens=lens, causal=causal, zigzag=zigzag, dtype="bf16")
