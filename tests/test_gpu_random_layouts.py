@@ -3,15 +3,21 @@
 
 Each case runs the forward and the backward through the C-ABI and compares every output and gradient element with
 the float64 oracle at the stated bounds.  bf16 cases also run the host-buffer forward, which must give the device
-forward's outputs bit for bit.  The layouts come from a fixed seed, so a failure names a reproducible case.
+forward's outputs bit for bit.  A second set of bf16 layouts runs ring attention with its D ranks held on one GPU
+(every rank's shard in buffers of its own, the K/V blocks passed round the ring; ShardTensor summary, section 4,
+ring attention) against the same oracle.  The layouts come from a fixed seed, so a failure names a reproducible
+case.
 """
 import numpy as np
 import pytest
 import torch
 
 import domain_ring_attention_gb300 as st
+from domain_ring_attention_gb300 import _lib
 from domain_ring_attention_gb300.workloads import Workload, make_inputs
-from gpu_common import assert_no_device_error, check_full, run_case
+from gpu_common import assert_close, assert_lse, assert_no_device_error, check_full, f64, run_case
+from oracle import attention as oa
+from oracle import layout as ol
 
 pytestmark = pytest.mark.gpu
 
@@ -59,3 +65,42 @@ def test_random_layout_forward_backward(i, B, H, d, lens, causal, zigzag, dtype)
     assert_no_device_error()
     assert torch.equal(out_h, res["out_native"].cpu())
     assert torch.equal(lse_h, res["lse"].cpu())
+
+
+def ring_cases(n=12, seed=20261204):
+    rng = np.random.RandomState(seed)
+    cases = []
+    for i in range(n):
+        D = int(rng.randint(1, 7))
+        zigzag = bool(rng.rand() < 0.5)
+        causal = bool(rng.rand() < 0.6)
+        if zigzag:
+            lens = tuple(int(2 * rng.randint(1, 201)) for _ in range(D))
+        else:
+            lens = tuple(int(rng.randint(1, 401)) for _ in range(D))
+        d = 64 if rng.rand() < 0.5 else 128
+        B, H = int(rng.randint(1, 3)), int(rng.randint(1, 3))
+        cases.append((i, B, H, d, lens, causal, zigzag))
+    return cases
+
+
+@pytest.mark.parametrize("i,B,H,d,lens,causal,zigzag", ring_cases())
+def test_random_layout_ring_on_one_gpu(i, B, H, d, lens, causal, zigzag):
+    wl = Workload("ring%d" % i, B=B, H=H, d=d, lens=lens, causal=causal, zigzag=zigzag, dtype="bf16")
+    q, k, v, do = (x.cuda() for x in make_inputs(wl, seed=2000 + i, with_dout=True))
+    lay = st.Layout(lens, zigzag)
+    off = ol.shard_offsets(list(lens))
+    qs, ks, vs, dos = ([x[:, off[r]:off[r + 1]].contiguous() for r in range(len(lens))] for x in (q, k, v, do))
+    outs, lses = _lib.st_ring_fwd_local(lay, qs, ks, vs, causal=causal, out_dtype=torch.float32)
+    dqs, dks, dvs = _lib.st_ring_bwd_local(lay, qs, ks, vs, outs, lses, dos, causal=causal)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    Q, K, V, DO = (f64(x) for x in (q, k, v, do))
+    ro, rl = oa.forward(Q, K, V, lens, zigzag, causal)
+    out = np.concatenate([f64(x) for x in outs], axis=1)
+    lse = np.concatenate([f64(x) for x in lses], axis=2)
+    assert_close(out, ro, "bf16", "out")
+    assert_lse(lse, rl, "bf16")
+    gq, gk, gv = oa.backward(Q, K, V, ro, rl, DO, lens, zigzag, causal)
+    for name, got, ref in (("dq", dqs, gq), ("dk", dks, gk), ("dv", dvs, gv)):
+        assert_close(np.concatenate([f64(x) for x in got], axis=1), ref, "bf16", name, rel_rms=True)
