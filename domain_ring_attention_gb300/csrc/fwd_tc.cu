@@ -403,22 +403,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto step = [&](bool split0, bool split1, bool fresh) {
                 const int s = j % C::kStages;
                 const uint64_t kd = kdesc + (uint64_t)(s * (C::kTileBytes >> 4));
-                ok = mbar_wait(bar_kv(s), (j / C::kStages) & 1, abort_flag);
-                if (!ok) return;
-                tc_fence_after();
-                if (j == 0) {
-                    for (int t = 0; t < kNQ; ++t) issue_s(t, kd);
-                } else {
-                    // V(j-1) landed with K(j-1), waited for one tile ago
-                    const int sp = (j - 1) % C::kStages;
-                    const uint64_t vd = vdesc + (uint64_t)(sp * (C::kVStageBytes >> 4));
-                    for (int t = 0; t < kNQ && ok; ++t) {
-                        pv_when_ready(t, vd, j - 1);
-                        if (!ok) break;
-                        issue_s(t, kd);
-                    }
+                if constexpr (C::kStages > 2) {
+                    ok = mbar_wait(bar_kv(s), (j / C::kStages) & 1, abort_flag);
                     if (!ok) return;
-                    mma_commit(bar_e(sp));
+                    tc_fence_after();
+                    if (j == 0) {
+                        for (int t = 0; t < kNQ; ++t) issue_s(t, kd);
+                    } else {
+                        // V(j-1) landed with K(j-1), waited for one tile ago
+                        const int sp = (j - 1) % C::kStages;
+                        const uint64_t vd = vdesc + (uint64_t)(sp * (C::kVStageBytes >> 4));
+                        for (int t = 0; t < kNQ && ok; ++t) {
+                            pv_when_ready(t, vd, j - 1);
+                            if (!ok) break;
+                            issue_s(t, kd);
+                        }
+                        if (!ok) return;
+                        mma_commit(bar_e(sp));
+                    }
+                } else {
+                    // Two K/V stages (d = 128): PV_0(j-1) needs only P_0(j-1) and
+                    // V(j-1), so it goes ahead of the wait for K(j), and the stage of
+                    // tile j-1 is released right after PV_1(j-1), its last reader, so
+                    // that the producer refills it while S_1(j) runs; otherwise the
+                    // next tile's load (~1000 clocks) starts only after every MMA of
+                    // this tile, and the tensor pipe idles while it lands.
+                    auto wait_kv = [&] {
+                        ok = mbar_wait(bar_kv(s), (j / C::kStages) & 1, abort_flag);
+                        if (ok) tc_fence_after();
+                    };
+                    if (j == 0) {
+                        wait_kv();
+                        if (!ok) return;
+                        for (int t = 0; t < kNQ; ++t) issue_s(t, kd);
+                    } else {
+                        const int sp = (j - 1) % C::kStages;
+                        const uint64_t vd = vdesc + (uint64_t)(sp * (C::kVStageBytes >> 4));
+                        for (int t = 0; t < kNQ && ok; ++t) {
+                            pv_when_ready(t, vd, j - 1);
+                            if (!ok) break;
+                            if (t == 0) {
+                                wait_kv();
+                                if (!ok) break;
+                            }
+                            if (t == kNQ - 1) mma_commit(bar_e(sp));
+                            issue_s(t, kd);
+                        }
+                        if (!ok) return;
+                    }
                 }
                 split_prev[0] = split0;
                 split_prev[1] = split1;
