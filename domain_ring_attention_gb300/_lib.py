@@ -116,9 +116,17 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
-def _stream(stream):
+def _stream(stream, *keep):
+    """The handle of the stream a call runs on.  ``keep``: device tensors the call's kernels use that this
+    binding allocated (workspaces, outputs).  The caching allocator ties a block to the stream that was current
+    at its allocation; when the call runs on another stream they are recorded on it, so that their memory is
+    not handed to other work before the call's kernels are done with it."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    held = [x for t in keep for x in (t if isinstance(t, (list, tuple)) else (t,)) if x is not None and x.is_cuda]
+    if held and stream != torch.cuda.current_stream(held[0].device):
+        for x in held:
+            x.record_stream(stream)
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -221,7 +229,7 @@ def st_attn_fwd(layout, q, k, v, causal=False, scale=0.0, out=None, lse=None, st
         workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
     _check(load().st_attn_fwd(layout.handle, B, H, d, _dtype_code(q.dtype), int(bool(causal)),
                               float(scale), _ptr(q), _ptr(k), _ptr(v), _dtype_code(odt), _ptr(out),
-                              _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)),
+                              _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream, out, lse, workspace)),
            "st_attn_fwd")
     return out, lse
 
@@ -255,8 +263,8 @@ def st_attn_fwd_host(layout, q_host, k_host, v_host, out_host, lse_host, dev, ca
     _check(load().st_attn_fwd_host(layout.handle, B, H, d, ST_DTYPE_BF16, int(bool(causal)), float(scale),
                                    _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(out_host), _ptr(lse_host),
                                    _ptr(dev["q"]), _ptr(dev["k"]), _ptr(dev["v"]), _ptr(dev["out"]),
-                                   _ptr(dev["lse"]), _ptr(workspace), workspace.numel(), _stream(stream),
-                                   _stream(copy_stream)), "st_attn_fwd_host")
+                                   _ptr(dev["lse"]), _ptr(workspace), workspace.numel(),
+                                   _stream(stream, workspace), _stream(copy_stream)), "st_attn_fwd_host")
     return out_host, lse_host
 
 
@@ -273,7 +281,7 @@ def st_attn_fwd_partials(layout, q, k, v, causal=False, scale=0.0, stream=None, 
     _check(load().st_attn_fwd_partials(layout.handle, B, H, d, _dtype_code(q.dtype),
                                        int(bool(causal)), float(scale), _ptr(q), _ptr(k), _ptr(v),
                                        _ptr(po), _ptr(pl), _ptr(workspace), workspace.numel(),
-                                       _stream(stream)), "st_attn_fwd_partials")
+                                       _stream(stream, po, pl, workspace)), "st_attn_fwd_partials")
     return po, pl
 
 
@@ -288,7 +296,7 @@ def st_attn_merge(partial_out, partial_lse, out_dtype=torch.float32, out=None, l
     if lse is None:
         lse = torch.empty((B, H, S), device=partial_out.device, dtype=torch.float32)
     _check(load().st_attn_merge(D, B, H, S, d, _ptr(partial_out), _ptr(partial_lse), _ptr(out),
-                                _ptr(lse), _dtype_code(out.dtype), _stream(stream)), "st_attn_merge")
+                                _ptr(lse), _dtype_code(out.dtype), _stream(stream, out, lse)), "st_attn_merge")
     return out, lse
 
 
@@ -315,7 +323,8 @@ def st_attn_bwd(layout, q, k, v, out, lse, dout, causal=False, scale=0.0, grad_d
                               float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
                               _dtype_code(out.dtype), _ptr(lse), _ptr(dout), _dtype_code(gdt),
                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
-                              workspace.numel() * workspace.element_size(), _stream(stream)),
+                              workspace.numel() * workspace.element_size(),
+                              _stream(stream, dq, dk, dv, workspace)),
            "st_attn_bwd")
     return dq, dk, dv
 
@@ -324,7 +333,7 @@ def st_permute(layout, x, to_natural=True, stream=None):
     B, S, H, d = _shape(x)
     out = torch.empty_like(x)
     _check(load().st_permute(layout.handle, B, H, d, _dtype_code(x.dtype), int(bool(to_natural)),
-                             _ptr(x), _ptr(out), _stream(stream)), "st_permute")
+                             _ptr(x), _ptr(out), _stream(stream, out)), "st_permute")
     return out
 
 
@@ -343,7 +352,8 @@ def st_proj_gemm(x, w, out_dtype=torch.bfloat16, out=None, stream=None):
         raise StAttnError(-8, "st_proj_gemm (weight shape)")
     if out is None:
         out = torch.empty(tuple(x.shape[:-1]) + (N,), device=x.device, dtype=out_dtype)
-    _check(load().st_proj_gemm(M, N, K, _ptr(x), _ptr(w), _ptr(out), _dtype_code(out.dtype), _stream(stream)),
+    _check(load().st_proj_gemm(M, N, K, _ptr(x), _ptr(w), _ptr(out), _dtype_code(out.dtype),
+                               _stream(stream, out)),
            "st_proj_gemm")
     return out
 
@@ -371,7 +381,7 @@ def st_gated_mlp(x, w1, w3, w2, out_dtype=torch.bfloat16, out=None, h=None, stre
     if out is None:
         out = torch.empty(tuple(x.shape[:-1]) + (hidden,), device=x.device, dtype=out_dtype)
     _check(load().st_gated_mlp(M, hidden, F, _ptr(x), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(h), _ptr(out),
-                               _dtype_code(out.dtype), _stream(stream)), "st_gated_mlp")
+                               _dtype_code(out.dtype), _stream(stream, out, h)), "st_gated_mlp")
     return out, h
 
 
@@ -428,7 +438,7 @@ def st_conv2d_sharded(shards, weight, bias=None, out_dtype=torch.bfloat16, out=N
         out = [torch.empty((max(L, 0), W, C_out), device=shards[0].device, dtype=out_dtype) for L in rows]
     D = len(shards)
     _check(load().st_conv2d_sharded(D, (_I64 * D)(*rows), W, C_in, C_out, k, _ptr_array(shards), _ptr(weight),
-                                    _ptr(bias), _ptr_array(out), _dtype_code(out[0].dtype), _stream(stream)),
+                                    _ptr(bias), _ptr_array(out), _dtype_code(out[0].dtype), _stream(stream, out)),
            "st_conv2d_sharded")
     return out
 
@@ -456,7 +466,7 @@ def st_group_norm_sharded(shards, G, gamma=None, beta=None, eps=1e-5, out_dtype=
     _check(lib.st_group_norm_sharded(D, (_I64 * D)(*rows), W, C, int(G), float(eps), _ptr_array(shards),
                                      _ptr(gamma), _ptr(beta), _ptr_array(out), int(out_pad),
                                      _dtype_code(out[0].dtype), _ptr(workspace), workspace.numel(),
-                                     _stream(stream)), "st_group_norm_sharded")
+                                     _stream(stream, out, workspace)), "st_group_norm_sharded")
     return out
 
 
@@ -490,7 +500,7 @@ def st_ring_fwd_step(layout, q_shard, kv_shard, q, k, v, prev=None, causal=False
     _check(load().st_ring_fwd_step(layout.handle, int(q_shard), int(kv_shard), B, H, d, ST_DTYPE_BF16,
                                    int(bool(causal)), float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(po), _ptr(pl),
                                    _dtype_code(out.dtype), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
-                                   _stream(stream)), "st_ring_fwd_step")
+                                   _stream(stream, out, lse, workspace)), "st_ring_fwd_step")
     return out, lse
 
 
@@ -504,7 +514,7 @@ def st_ring_bwd_step(layout, q_shard, kv_shard, q, k, v, out, lse, dout, dq, dk,
     _check(load().st_ring_bwd_step(layout.handle, int(q_shard), int(kv_shard), B, H, d, ST_DTYPE_BF16,
                                    int(bool(causal)), float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
                                    _dtype_code(out.dtype), _ptr(lse), _ptr(dout), int(bool(first_q)), _ptr(dq),
-                                   _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), _stream(stream)),
+                                   _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), _stream(stream, workspace)),
            "st_ring_bwd_step")
     return dq, dk, dv
 
@@ -528,7 +538,8 @@ def st_ring_fwd_local(layout, qs, ks, vs, causal=False, scale=0.0, out_dtype=tor
         copy_stream = torch.cuda.Stream(device=dev)
     _check(load().st_ring_fwd_local(layout.handle, B, H, d, int(bool(causal)), float(scale), _ptrs(qs), _ptrs(ks),
                                     _ptrs(vs), _dtype_code(out_dtype), _ptrs(outs), _ptrs(lses), _ptr(workspace),
-                                    workspace.numel(), _stream(stream), _stream(copy_stream)), "st_ring_fwd_local")
+                                    workspace.numel(), _stream(stream, outs, lses, workspace), _stream(copy_stream)),
+           "st_ring_fwd_local")
     return outs, lses
 
 
@@ -547,7 +558,7 @@ def st_ring_bwd_local(layout, qs, ks, vs, outs, lses, douts, causal=False, scale
     _check(load().st_ring_bwd_local(layout.handle, B, H, d, int(bool(causal)), float(scale), _ptrs(qs), _ptrs(ks),
                                     _ptrs(vs), _ptrs(outs), _dtype_code(outs[0].dtype), _ptrs(lses), _ptrs(douts),
                                     _ptrs(dqs), _ptrs(dks), _ptrs(dvs), _ptr(workspace), workspace.numel(),
-                                    _stream(stream), _stream(copy_stream)), "st_ring_bwd_local")
+                                    _stream(stream, dqs, dks, dvs, workspace), _stream(copy_stream)), "st_ring_bwd_local")
     return dqs, dks, dvs
 
 
@@ -559,7 +570,7 @@ def st_attn_bwd_delta(out, dout, delta=None, stream=None):
     if delta is None:
         delta = torch.empty((B, H, S), device=dout.device, dtype=torch.float32)
     _check(load().st_attn_bwd_delta(B, H, S, d, _dtype_code(dout.dtype), _ptr(out), _dtype_code(out.dtype),
-                                    _ptr(dout), _ptr(delta), _stream(stream)), "st_attn_bwd_delta")
+                                    _ptr(dout), _ptr(delta), _stream(stream, delta)), "st_attn_bwd_delta")
     return delta
 
 
@@ -567,7 +578,7 @@ def st_convert_f32(src, dtype=torch.bfloat16, out=None, stream=None):
     """fp32 tensor -> ``dtype`` (bf16 rounded to nearest even, or an fp32 copy)."""
     if out is None:
         out = torch.empty(src.shape, device=src.device, dtype=dtype)
-    _check(load().st_convert_f32(src.numel(), _ptr(src), _ptr(out), _dtype_code(out.dtype), _stream(stream)),
+    _check(load().st_convert_f32(src.numel(), _ptr(src), _ptr(out), _dtype_code(out.dtype), _stream(stream, out)),
            "st_convert_f32")
     return out
 
@@ -581,5 +592,5 @@ def st_fp16_scaled_copy(src, out=None, exps=None, scratch=None, stream=None):
     if scratch is None:
         scratch = torch.zeros(4, device=src.device, dtype=torch.int32)
     _check(load().st_fp16_scaled_copy(src.numel(), _ptr(src), _ptr(out), _ptr(exps), _ptr(scratch),
-                                      _stream(stream)), "st_fp16_scaled_copy")
+                                      _stream(stream, out, exps, scratch)), "st_fp16_scaled_copy")
     return out, exps
