@@ -441,6 +441,15 @@ extern "C" int st_attn_fwd_host(const st_layout_t* L, int B, int H, int d, int d
         if ((int64_t)t.ntiles * B * (H / g) < 4LL * std::max(sms, 1)) break;
         hn = H / g;
     }
+    // H without such a divisor (a prime, say): the fewest heads that make four
+    // waves, and at least (H - 2) / 16 (at most 18 groups: the workspace holds
+    // 32 exponents), when the whole problem spans eight waves or more
+    const int64_t per_head = (int64_t)t.ntiles * B;
+    if (hn == H && H >= 4 && per_head * H >= 8LL * std::max(sms, 1)) {
+        int want = (int)((4LL * std::max(sms, 1) + per_head - 1) / per_head);
+        want = std::max(want, (H - 2 + 15) / 16);
+        if (want <= H - 2) hn = want;
+    }
     if (hn < H)
         return fwd_host_groups(L, t, B, H, d, causal, scale, hn, q_host, k_host, v_host, out_host, lse_host, q, k,
                                v, out, lse, workspace, need, stream, copy_stream);

@@ -140,7 +140,10 @@ int st_attn_fwd(const st_layout_t* layout, int B, int H, int d, int dtype, int c
  * split by heads where it can be:
  *   - Head groups, when H has a divisor G (2 <= G <= 16) whose groups of
  *     hn = H / G heads still launch at least four waves of CTAs (the largest
- *     such G): a single head first and last, groups of up to hn heads between.
+ *     such G), or, for H >= 4 without one, when the whole problem spans eight
+ *     waves or more (hn: the fewest heads that make four waves, at least
+ *     (H - 2) / 16): a single head first and last, groups of up to hn heads
+ *     between.
  *     Per group, V, K and Q of its heads are copied in on copy_stream (2-D
  *     copies, pitch H * d); the fp16 copy of its V (with a scale of its own)
  *     and its attention launch run once they have landed, on `stream` and on

@@ -9,7 +9,7 @@ normalisation then differ by exact powers of two only, so the outputs are still 
 - head groups of 1, 4, 4, 4, 2 and 1 heads;
 - causal zigzag over uneven shards in head groups of 1, 16, 14 and 1 (heaviest tiles first within each group);
 - three chunks of query tiles (H = 3 has no divisor that leaves four waves per group);
-- head groups of uneven sizes (1, 3, 1, 1 for H = 6);
+- head groups of uneven sizes (1, 3, 1, 1 for H = 6; 1, 3, 2, 1 for H = 7, which has no divisor);
 - causal zigzag at d = 64 in head groups of 1, 2, 2, 2, 1.
 A few rows are also held to the oracle with the bf16 bounds.
 """
@@ -33,6 +33,7 @@ pytestmark = pytest.mark.gpu
     (2, 3, 64, (8192,) * 8, False, False),             # three chunks of query tiles: 51 + 154 + 51
     (1, 6, 64, (16384,) * 4, False, False),            # head groups of 1, 3, 1, 1
     (2, 8, 64, (12288, 20480, 4096, 2048), True, True),  # head groups of 1, 2, 2, 2, 1; causal zigzag, d = 64
+    (1, 7, 128, (8192,) * 8, False, False),            # H = 7 (no divisor): head groups of 1, 3, 2, 1
 ])
 def test_host_forward_equals_device_forward(B, H, d, lens, causal, zigzag):
     wl = Workload("host", B=B, H=H, d=d, lens=lens, causal=causal, zigzag=zigzag, dtype="bf16")
