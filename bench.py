@@ -472,12 +472,18 @@ def train_step_tflops(st, world, steps=3, warmup=2, name="train_s32768"):
         tb += ev[1].elapsed_time(ev[2])
     tf = max_over_ranks(tf / steps, world)
     tb = max_over_ranks(tb / steps, world)
-    return {"workload": name, "shard_lens": list(wl.lens), "causal": wl.causal, "zigzag": wl.zigzag,
+    res = {"workload": name, "shard_lens": list(wl.lens), "causal": wl.causal, "zigzag": wl.zigzag,
             "fwd_tflops": wl.fwd_flops() * world / (tf * 1e-3) / 1e12,
             "bwd_tflops": wl.bwd_flops() * world / (tb * 1e-3) / 1e12,
             "fwd_bwd_tflops": (wl.fwd_flops() + wl.bwd_flops()) * world / ((tf + tb) * 1e-3) / 1e12,
             "fwd_ms": tf, "bwd_ms": tb,
             "note": "fwd writes fp32 out (the backward's Delta); bwd writes fp32 dq, dk, dv"}
+    peak_b, _, _, kind = peaks()
+    for key in ("fwd", "bwd", "fwd_bwd"):
+        res[key + "_frac"] = res[key + "_tflops"] / world / peak_b
+    res["peak_tflops"] = peak_b
+    res["peak_kind"] = kind + " burst bf16 (fractions per GPU)"
+    return res
 
 
 def ring_local_tflops(st, world, steps=3, warmup=2, name="train_s32768"):
