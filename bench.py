@@ -459,17 +459,19 @@ def train_step_tflops(st, world, steps=3, warmup=2, name="train_s32768"):
         bwd()
     torch.cuda.synchronize()
     barrier(world)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    tf = tb = 0.0
-    for _ in range(steps):
-        ev[0].record(stream)
+    # the steps are queued back to back, as a training loop queues them (the host
+    # runs ahead of the GPU), with events around each pass, read after one
+    # synchronize; a small problem is then not charged the host's launch latency
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in ev:
+        e[0].record(stream)
         fwd()
-        ev[1].record(stream)
+        e[1].record(stream)
         bwd()
-        ev[2].record(stream)
-        torch.cuda.synchronize()
-        tf += ev[0].elapsed_time(ev[1])
-        tb += ev[1].elapsed_time(ev[2])
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    tf = sum(e[0].elapsed_time(e[1]) for e in ev)
+    tb = sum(e[1].elapsed_time(e[2]) for e in ev)
     tf = max_over_ranks(tf / steps, world)
     tb = max_over_ranks(tb / steps, world)
     res = {"workload": name, "shard_lens": list(wl.lens), "causal": wl.causal, "zigzag": wl.zigzag,

@@ -285,6 +285,28 @@ struct Fp16Job {
     int64_t n8[4];     // 8-element units of each tensor (n8 of the launch = the largest)
 };
 
+// Block-wide max of each thread's m[t] (all >= 0), then one atomicMax per block
+// and tensor on the float bits: a same-address atomic from every warp of a
+// full grid would serialise in L2 (about 10 us for the ~10^4 warps of one launch).
+template <int NT>
+__device__ __forceinline__ void block_amax(const float (&m)[NT], unsigned* __restrict__ amax_bits) {
+    __shared__ float part[NT][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        float v = m[t];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+        if (lane == 0) part[t][warp] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < NT) {
+        float v = part[threadIdx.x][0];
+        for (int w = 1; w < nw; ++w) v = fmaxf(v, part[threadIdx.x][w]);
+        atomicMax(amax_bits + threadIdx.x, __float_as_uint(v));
+    }
+}
+
 // max |x| of NT bf16 tensors of job.n8[t] * 8 elements each (float bits, atomicMax)
 template <int NT>
 __global__ void __launch_bounds__(256)
@@ -305,13 +327,7 @@ amax_kernel(int64_t n8, const __grid_constant__ Fp16Job job, unsigned* __restric
             }
         }
     }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        float v = m[t];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if ((threadIdx.x & 31) == 0) atomicMax(amax_bits + t, __float_as_uint(v));
-    }
+    block_amax<NT>(m, amax_bits);
 }
 
 // fp16 copies dst[t] = src[t] * 2^-e_t, exact; the exponents go to exps[0..NT).
@@ -370,9 +386,8 @@ amax_rows_kernel(int64_t nrows, int row8, int64_t pitch8, const uint4* __restric
             }
         }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (lane == 0) atomicMax(amax_bits, __float_as_uint(m));
+    const float mm[1] = {m};
+    block_amax<1>(mm, amax_bits);
 }
 
 // dst = src * 2^-e over the same strided rows (exact fp16), e -> exps[0]
