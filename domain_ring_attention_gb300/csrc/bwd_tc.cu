@@ -19,11 +19,13 @@
 //   dQ  += scale dQ_t       (softmax warps: TMEM -> the dS^T lo tile -> TMA bulk reduction)
 //
 // Warp roles (384 threads): warp 0 TMA producer (+ lse / Delta staging),
-// warp 1 TMEM allocator + MMA issuer, warps 4-7 softmax for query columns
-// 0-63 (one key row per thread), half of the dQ reduction (one query row per
-// thread) and the dV epilogue, warps 8-11 the same for columns 64-127 and the
-// dK epilogue.  Tensor memory: S^T|P^T, dP^T|dQ_t, dV, dK.  Every barrier
-// wait is bounded (tc_ptx.cuh).
+// warp 1 TMEM allocator + MMA issuer (at d = 64 with warp 2 as a second
+// issuer: dP^T and dK), warps 4-7 softmax for query columns 0-63 (one key row
+// per thread), half of the dQ reduction (one query row per thread) and the dV
+// epilogue, warps 8-11 the same for columns 64-127 and the dK epilogue.
+// Tensor memory: S^T|P^T, dP^T|dQ_t, dV, dK at d = 128; at d = 64 dQ_t has two
+// buffers of its own after dK, and a tile's dQ drain runs after the next
+// tile's softmax pass.  Every barrier wait is bounded (tc_ptx.cuh).
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -73,6 +75,17 @@ struct Cfg {
     static constexpr uint32_t kColDP = 128;
     static constexpr uint32_t kColDV = 256;
     static constexpr uint32_t kColDK = 256 + D;
+    // d = 64: dQ_t in two buffers of its own (columns 384-447, 448-511, by
+    // query-tile parity), so the next dP^T need not wait for the drain, and the
+    // drain of tile i can run after the softmax pass of tile i + 1.  At d = 128
+    // dQ_t reuses the dP^T columns.
+    static constexpr bool kOwnDq = D == 64;
+    static constexpr uint32_t kColDQ = 256 + 2 * D;
+    // d = 64: the MMAs are issued by two threads (warps 1 and 2), since one
+    // thread issues an N = 64 MMA more slowly than the tensor core runs it;
+    // the barriers the MMAs signal then count one commit from each.
+    static constexpr bool kTwoIss = D == 64;
+    static constexpr int kIss = kTwoIss ? 2 : 1;
 };
 
 // Operands: exact fp16 copies of q, k, v, dO scaled by 2^-e (e per tensor,
@@ -206,13 +219,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(bar_kv, 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar_qf(s), 2);     // the TMA bytes' arrival + the producer warp's statistics
-            mbar_init(bar_qe(s), 1);
+            mbar_init(bar_qe(s), C::kIss);
         }
-        mbar_init(bar_s, 1);
+        mbar_init(bar_s, C::kIss);
         mbar_init(bar_ds, 8);       // one arrival per softmax warp
-        mbar_init(bar_it, 1);
+        mbar_init(bar_it, C::kIss);
         mbar_init(bar_dqf, 8);
-        mbar_init(bar_drain, 1);
+        mbar_init(bar_drain, C::kIss);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -282,8 +295,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 mbar_wait_drain(bar_qf(ii % C::kStages), (ii / C::kStages) & 1);
         }
         (void)issued_tx;
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp == 1 || (C::kTwoIss && warp == 2)) {
+        // ------------------------------------------------ MMA issuer(s)
+        // Two issuing threads at d = 64: warp 1 (role a) issues S^T, dV and
+        // dQ_t, warp 2 dP^T and dK.  On tiles with hi + lo parts warp 1 also
+        // issues dK, and the next dP^T (which overwrites the P_lo columns that
+        // its dV MMAs read): the MMAs of one thread run in issue order, those of
+        // two threads do not.  Every other shared operand or accumulator is
+        // ordered through the barriers: a commit tracks all earlier MMAs of its
+        // own thread, and each barrier waits for both threads' commits.
+        const bool role_a = warp == 1;
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_f16_f32(kT, kT, 0, 0);      // S^T, dP^T
             constexpr uint32_t id_kv = idesc_f16_f32(kT, D, 0, 1);      // dV, dK (B MN-major)
@@ -308,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             bool ok = mbar_wait(bar_kv, 0, abort_flag);
             tc_fence_after();
             int i = 0;
+            bool prev_split = false;
             ring_walk_q(p.qtab, kt.shard, [&](int, int nq, int natq) {
                 if (!ok || !active(nq, natq)) return;
                 const int s = i % C::kStages;
@@ -319,17 +341,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 ok = mbar_wait(bar_qf(s), (i / C::kStages) & 1, abort_flag);
                 if (!ok) return;
                 tc_fence_after();
+                if (role_a) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + C::kColS, k_k + koff(kk), q_k + st + koff(kk), id_s, kk > 0);
-                if (i > 0) {
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + C::kColS, k_k + koff(kk), q_k + st + koff(kk), id_s, kk > 0);
+                }
+                if (!C::kOwnDq && i > 0) {
                     ok = mbar_wait(bar_dqf, (i - 1) & 1, abort_flag);
                     if (!ok) return;
                     tc_fence_after();
                 }
+                if (!C::kTwoIss || role_a == prev_split) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + C::kColDP, v_k + koff(kk), o_k + st + koff(kk), id_s, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + C::kColDP, v_k + koff(kk), o_k + st + koff(kk), id_s, kk > 0);
+                }
                 mma_commit(bar_s);
                 ok = mbar_wait(bar_ds, i & 1, abort_flag);
                 if (!ok) return;
@@ -341,36 +367,47 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 // columns, dS_lo in a second smem tile) and every product gets
                 // a second MMA for the lo part.
                 const bool split = wants_split(classify(causal, natq, nq, kt.nat0, kt.nq, kT), natq);
-                // dV += P^T dO  (A: P^T fp16 in TMEM; B: dO, K = query rows, N = D)
-#pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk)
-                    mma_ts(tmem + C::kColDV, tmem + C::kColS + pk(kk), o_mn + st + moff(kk), id_kv,
-                           (!seg_start(i) || kk > 0) ? 1u : 0u);
-                if (split) {
+                if (role_a) {
+                    // dV += P^T dO  (A: P^T fp16 in TMEM; B: dO, K = query rows, N = D)
 #pragma unroll
                     for (int kk = 0; kk < kT / 16; ++kk)
-                        mma_ts(tmem + C::kColDV, tmem + C::kColDP + pk(kk), o_mn + st + moff(kk), id_kv, 1u);
+                        mma_ts(tmem + C::kColDV, tmem + C::kColS + pk(kk), o_mn + st + moff(kk), id_kv,
+                               (!seg_start(i) || kk > 0) ? 1u : 0u);
+                    if (split) {
+#pragma unroll
+                        for (int kk = 0; kk < kT / 16; ++kk)
+                            mma_ts(tmem + C::kColDV, tmem + C::kColDP + pk(kk), o_mn + st + moff(kk), id_kv, 1u);
+                    }
                 }
                 // dK += dS^T Q  (A: dS^T K-major in smem; B: Q, K = query rows, N = D)
-                for (int part = 0; part < (split ? 2 : 1); ++part) {
+                if (!C::kTwoIss || role_a == split) {
+                    for (int part = 0; part < (split ? 2 : 1); ++part) {
 #pragma unroll
-                    for (int kk = 0; kk < kT / 16; ++kk)
-                        mma_ss(tmem + C::kColDK, ds_k[part] + koff(kk), q_mn + st + moff(kk), id_kv,
-                               (!seg_start(i) || kk > 0 || part > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kT / 16; ++kk)
+                            mma_ss(tmem + C::kColDK, ds_k[part] + koff(kk), q_mn + st + moff(kk), id_kv,
+                                   (!seg_start(i) || kk > 0 || part > 0) ? 1u : 0u);
+                    }
                 }
                 // Q(i) and dO(i) are read by no later MMA: the producer may refill
                 // the stage while dQ_t runs.
                 mma_commit(bar_qe(s));
                 // dQ_t = dS K  (A: dS, M = query rows contiguous; B: K, K = keys, N = D).
-                // It overwrites the P_lo columns, which the dV MMA above read
-                // first (tcgen05.mma operations of one thread run in order).
-                for (int part = 0; part < (split ? 2 : 1); ++part) {
+                // d = 128: it overwrites the P_lo columns, which the dV MMA above
+                // read first (tcgen05.mma operations of one thread run in order).
+                // d = 64: buffer i & 1 of its own, whose previous tile (i - 2)
+                // every softmax warp has drained before its "dS ready" arrival
+                // of tile i (the drain of tile i - 2 precedes the pass of tile i).
+                const uint32_t col_dq = C::kOwnDq ? C::kColDQ + (uint32_t)(i & 1) * D : C::kColDP;
+                if (role_a) {
+                    for (int part = 0; part < (split ? 2 : 1); ++part) {
 #pragma unroll
-                    for (int kk = 0; kk < kT / 16; ++kk)
-                        mma_ss(tmem + C::kColDP, ds_mn[part] + moff(kk), k_mn + moff(kk), id_q,
-                               (kk > 0 || part > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kT / 16; ++kk)
+                            mma_ss(tmem + col_dq, ds_mn[part] + moff(kk), k_mn + moff(kk), id_q,
+                                   (kk > 0 || part > 0) ? 1u : 0u);
+                    }
                 }
                 mma_commit(bar_it);
+                prev_split = split;
                 ++i;
             });
             mma_commit(bar_drain);
@@ -528,19 +565,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
         // dQ_t of the tile whose MMAs just finished -> dq_acc (group 1)
         // dQ_t of the tile whose MMAs just finished -> dq_acc; each group
         // takes half of the columns (one query row per thread)
-        auto drain = [&](int q0, int nq) {
+        // `it`: the tile's index among the active ones (its dQ_t buffer at d = 64);
+        // `late`: the drain runs after the next tile's softmax pass (d = 64), while
+        // that tile's MMAs may read the dS^T lo tile, so it stages only in the
+        // warp's own slice.
+        auto drain = [&](int q0, int nq, int it, bool late) {
             // This group's columns of the row come into registers first and
-            // the TMEM is released at once (the next dP^T waits for both
-            // groups); the reductions then overlap that MMA.
+            // the TMEM is released at once (at d = 128 the next dP^T waits for
+            // both groups); the reductions then overlap the MMAs.
             constexpr int kCols = D / 2;
+            const uint32_t col = C::kOwnDq ? C::kColDQ + (uint32_t)(it & 1) * D : C::kColDP;
             uint32_t v[kCols];
 #pragma unroll
             for (int c = 0; c < kCols / 32; ++c)
-                tmem_ld32(lane_base + C::kColDP + grp * kCols + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+                tmem_ld32(lane_base + col + grp * kCols + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_dqf);
+            if (!C::kOwnDq && lane == 0) mbar_arrive(bar_dqf);
             // The reductions go through the TMA: per 32-column chunk the warp
             // writes its 32 rows into a 128-byte-swizzled fp32 tile (rows past
             // the query tile as zeros, which add nothing) and one lane issues a
@@ -550,10 +592,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
             for (int c = 0; c < kCols / 32; ++c) {
                 // the TMA has read this slice's previous chunk out of it; the other
-                // slice's (most recent) group may still be reading
-                if (lane == 0) bulk_wait_read_1();
+                // slice's (most recent) group may still be reading.  A late drain
+                // uses only the warp's own slice.
+                if (lane == 0) {
+                    if (late)
+                        bulk_wait_read_0();
+                    else
+                        bulk_wait_read_1();
+                }
                 __syncwarp();
-                const uint32_t buf = (nch++ & 1) ? stg2 : stg;
+                const uint32_t buf = late ? stg2 : ((nch++ & 1) ? stg2 : stg);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     // 16-byte unit k of row `lane` under the 128-byte swizzle
@@ -573,6 +621,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
                 }
             }
         };
+        // d = 64 (unless the CTA flushes its accumulators): the drain of tile i
+        // runs after the softmax pass of tile i + 1, while that tile's MMAs run.
+        // Waiting for S^T and dP^T of tile i + 1 also waits for every MMA of
+        // tile i (a commit tracks all earlier MMAs of its thread).
+        const bool late = C::kOwnDq && !flush_tile;
+        int pq0 = 0, pnq = 0;    // the tile whose drain is pending (late)
         int i = 0;
         bool ok = true;
         ring_walk_q(p.qtab, kt.shard, [&](int q0, int nq, int natq) {
@@ -616,14 +670,29 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const __grid_consta
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_ds);
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_it, i & 1, abort_flag));
-            if (!ok) return;
-            tc_fence_after();
-            drain(q0, nq);
+            if (late) {
+                if (i > 0) drain(pq0, pnq, i - 1, true);
+                pq0 = q0;
+                pnq = nq;
+            } else {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar_it, i & 1, abort_flag));
+                if (!ok) return;
+                tc_fence_after();
+                drain(q0, nq, i, false);
+            }
             ++i;
         });
+        if (ok && late && i > 0) {
+            // the last tile: all MMAs of the CTA done (the issuer's final
+            // commit, a barrier of a single phase)
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_drain, 0, abort_flag));
+            if (ok) {
+                tc_fence_after();
+                drain(pq0, pnq, i - 1, true);
+            }
+        }
         // epilogue: dV (group 0) or scale * dK (group 1) for this key row (the
-        // last tile's MMAs were waited for in its drain)
+        // last tile's MMAs were waited for before its drain)
         if (ok) {
             tc_fence_after();
             emit(i > 0, flushed || p.accum);
