@@ -42,7 +42,8 @@ def half_ulp_bf16(x):
     return np.where(x == 0, 0.0, np.ldexp(1.0, e - 9))
 
 
-def test_backward_determinism_and_bf16_gradients():
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_determinism_and_bf16_gradients(d):
     """Two backward runs and a bf16-gradient run of the same case, all held to the oracle.
 
     dK and dV of a key tile are accumulated by one CTA, query tile after query tile in a fixed order, so they
@@ -50,8 +51,9 @@ def test_backward_determinism_and_bf16_gradients():
     per key tile, as here, the fp32 path takes no intermediate sums either).  dQ is added into an fp32
     accumulator by TMA reductions from the CTAs of all key tiles, in an order that varies from run to run, so
     it is not bitwise reproducible: its bf16 value is compared with the oracle, allowing half a bf16 spacing
-    on top of the fp32 bound."""
-    wl = Workload("small", B=1, H=3, d=128, lens=(256, 128, 384), causal=True, zigzag=True, dtype="bf16")
+    on top of the fp32 bound.  At d = 64 two threads issue the MMAs (dK by either, ordered through barriers),
+    and with bf16 gradients the dQ drain runs one tile late; neither may change dK or dV by a bit."""
+    wl = Workload("small", B=1, H=3, d=d, lens=(256, 128, 384), causal=True, zigzag=True, dtype="bf16")
     res_a = run_case(wl, seed=3)
     res_b = run_case(wl, seed=3)
     res16 = run_case(wl, seed=3, grad_dtype=torch.bfloat16)
@@ -70,6 +72,26 @@ def test_backward_determinism_and_bf16_gradients():
     rms = float(np.sqrt(np.mean(rq * rq)))
     excess = np.maximum(np.abs(got - rq) - half_ulp_bf16(got), 0.0) / rms
     assert excess.max() <= 1e-2 and excess.mean() <= 1e-3, (excess.max(), excess.mean())
+
+
+def test_d64_causal_bf16_gradients_many_tiles():
+    """d = 64, causal zigzag over uneven shards, bf16 gradients, 24 query tiles per key tile.
+
+    This covers the d = 64 schedule where the dQ drain of a tile runs after the next tile's softmax pass.
+    With bf16 gradients the lead key tile has no intermediate fp32 flushes, and it is split into hi + lo
+    parts on every tile, so dK and the next dP^T are issued by the first thread there.  All three gradients
+    are held to the oracle at the fp32 bound plus half a bf16 spacing."""
+    wl = Workload("d64long", B=1, H=2, d=64, lens=(1536, 1024, 512), causal=True, zigzag=True, dtype="bf16")
+    res = run_case(wl, seed=8, grad_dtype=torch.bfloat16)
+    q, k, v, do = (f64(x) for x in res["in"])
+    ro, rl = oa.forward(q, k, v, wl.lens, wl.zigzag, wl.causal)
+    ref = oa.backward(q, k, v, ro, rl, do, wl.lens, wl.zigzag, wl.causal)
+    for name, g, r in zip(("dq", "dk", "dv"), res["grads"], ref):
+        assert g.dtype == torch.bfloat16
+        got = f64(g)
+        rms = float(np.sqrt(np.mean(r * r)))
+        excess = np.maximum(np.abs(got - r) - half_ulp_bf16(got), 0.0) / rms
+        assert excess.max() <= 1e-2 and excess.mean() <= 1e-3, (name, excess.max(), excess.mean())
 
 
 def test_backward_with_bf16_out():
