@@ -163,6 +163,70 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// The softmax pass of a tile on the causal diagonal, one row per lane: P =
+// 2^(S * sl2 - m_ref) split into fp16 hi and lo parts (P = P_hi + P_lo, P_hi
+// over S's columns 0-63, P_lo over columns 64-127; keys past `limit` masked).
+// Returns the row's sum of P over the tile (kSum).  Not inlined: inlined into
+// the softmax loop, the registers of the two parts made the compiler spill on
+// every tile of the causal kernels, not only on these (the forward ran ~8 %
+// slower).  S is read again from tensor memory, columns 64-127 (where P_lo
+// goes) first, so that no store of this pass overwrites scores not yet read.
+// With kHalfP (d = 64) the keys 0-63 signal goes out halfway, as in the
+// ordinary pass; the caller has rescaled O before.
+template <bool kSum, bool kHalfP>
+__device__ __noinline__ float diag_pass(uint32_t tS, float sl2, float m_ref, int limit, uint32_t bar_half) {
+    uint32_t s23[2][32];
+    tmem_ld32(tS + 64, s23[0]);
+    tmem_ld32(tS + 96, s23[1]);
+    tmem_wait_ld();
+    const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_ref, -m_ref);
+    uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t s01[32];
+        if (c < 2) {
+            tmem_ld32(tS + c * 32, s01);
+            tmem_wait_ld();
+        }
+        if (kHalfP && c == 2) {
+            // keys 0-63 (hi and lo parts) are written
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(bar_half);
+        }
+        uint32_t pk[16], pl[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int k = 32 * c + 2 * i;
+            const uint32_t u0 = c < 2 ? s01[2 * i] : s23[c & 1][2 * i];
+            const uint32_t u1 = c < 2 ? s01[2 * i + 1] : s23[c & 1][2 * i + 1];
+            const float v0 = k > limit ? -INFINITY : __uint_as_float(u0);
+            const float v1 = k + 1 > limit ? -INFINITY : __uint_as_float(u1);
+            float x0, x1;
+            f2_unpack(ffma2(f2_pack(v0, v1), sl2x2, negm2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            if constexpr (kSum) {
+                if (i & 1)
+                    acc1 = fadd2(acc1, f2_pack(p0, p1));
+                else
+                    acc0 = fadd2(acc0, f2_pack(p0, p1));
+            }
+            pk[i] = pack_f16(p0, p1);
+            const float2 hi = __half22float2(__floats2half2_rn(p0, p1));
+            pl[i] = pack_f16(p0 - hi.x, p1 - hi.y);
+        }
+        tmem_st16(tS + c * 16, pk);
+        tmem_st16(tS + 64 + c * 16, pl);
+    }
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+    if constexpr (kSum) {
+        f2_unpack(acc0, a0, a1);
+        f2_unpack(acc1, b0, b1);
+    }
+    return (a0 + a1) + (b0 + b1);
+}
+
 // Kind of the (query half, KV tile) pair; an empty half skips everything.
 __device__ __forceinline__ int half_kind(int causal, int nat0, int nq, int natk, int nk) {
     if (nq <= 0) return kSkip;
@@ -625,9 +689,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
                 tmem_wait_ld();
+                int limit = nk - 1;   // the last key this row sees in the tile
+                if (causal) limit = min(limit, natq - natk);
                 if (kind == kPartial) {
-                    int limit = nk - 1;
-                    if (causal) limit = min(limit, natq - natk);
 #pragma unroll
                     for (int c = 0; c < kN; ++c)
                         if (c > limit) sr[c >> 5][c & 31] = 0xff800000u;   // -inf
@@ -656,11 +720,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t sl2x2 = f2_pack(sl2, sl2);
                 const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
                 uint64_t acc0 = 0, acc1 = 0;   // two packed partial sums (0.0f bits)
-                // Two compile-time variants of the exponential pass, so the full
-                // tiles run without the split code: tiles on the causal
-                // diagonal write P = P_hi + P_lo, both fp16 (see issue_pv).
-                auto exp_pass = [&](auto split_tag) {
-                    constexpr bool kLo = decltype(split_tag)::value;
+                // The ordinary pass; tiles on the causal diagonal write P =
+                // P_hi + P_lo, both fp16 (see issue_pv), in diag_pass.
+                auto exp_pass = [&] {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         if (C::kHalfP && c == 2) {
@@ -671,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_fence_before();
                             warp_arrive(bar_pa(t));
                         }
-                        uint32_t pk[16], pl[16];
+                        uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const uint64_t x = ffma2(
@@ -688,37 +750,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pk[i] = pack_f16(p0, p1);
                         }
                         tmem_st16(tS + c * 16, pk);
-                        if constexpr (kLo) {
-                            // second pass over the chunk for the lo parts: the
-                            // exponentials are recomputed (diagonal tiles only)
-                            // rather than kept alive next to the hi parts
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const uint64_t x = ffma2(
-                                    f2_pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2x2, negm2);
-                                float x0, x1;
-                                f2_unpack(x, x0, x1);
-                                const float p0 = ex2(x0), p1 = ex2(x1);
-                                const float2 hi = __half22float2(__floats2half2_rn(p0, p1));
-                                pl[i] = pack_f16(p0 - hi.x, p1 - hi.y);
-                            }
-                            tmem_st16(tS + kN / 2 + c * 16, pl);
-                        }
                     }
                 };
-                if constexpr (kSplit) {
-                    if (kind == kPartial && on_diagonal(causal, nat_h[t], natk, nk))
-                        exp_pass(std::true_type{});
-                    else
-                        exp_pass(std::false_type{});
+                bool diag = false;
+                if constexpr (kSplit) diag = kind == kPartial && on_diagonal(causal, nat_h[t], natk, nk);
+                if (diag) {
+                    if constexpr (C::kHalfP) {
+                        // O_t is rescaled before PV_t(j) may start on keys 0-63
+                        if (__any_sync(0xffffffffu, resc) && j > 0) rescale_o(alpha);
+                    }
+                    const float tile_sum = diag_pass<!C::kSumCol, C::kHalfP>(tS, sl2, m_ref, limit, bar_pa(t));
+                    if constexpr (!C::kSumCol) l = l * alpha + tile_sum;
                 } else {
-                    exp_pass(std::false_type{});
-                }
-                float a0, a1, b0, b1;
-                if constexpr (!C::kSumCol) {
-                    f2_unpack(acc0, a0, a1);
-                    f2_unpack(acc1, b0, b1);
-                    l = l * alpha + ((a0 + a1) + (b0 + b1));
+                    exp_pass();
+                    float a0, a1, b0, b1;
+                    if constexpr (!C::kSumCol) {
+                        f2_unpack(acc0, a0, a1);
+                        f2_unpack(acc1, b0, b1);
+                        l = l * alpha + ((a0 + a1) + (b0 + b1));
+                    }
                 }
                 m = m_use;
             }
