@@ -41,8 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 # default workload (16 heads), from the committed ncu capture of the kernel
 # version named here; a kernel change without a new capture must drop its entry
 # (traffic is then null).
-NCU_TRAFFIC_BYTES = {"fwd_tc@5e2a69f": 422008832.0 + 123259648.0}
-KERNEL_VERSION = "fwd_tc@5e2a69f"
+NCU_TRAFFIC_BYTES = {"fwd_tc@6de3400": 423772672.0 + 123840000.0}
+KERNEL_VERSION = "fwd_tc@6de3400"
 DEFAULT_WORKLOAD = "vit4096_s65536"
 
 
