@@ -16,9 +16,16 @@ def f64(t):
     return t.detach().float().cpu().double().numpy()
 
 
-def assert_close(got, ref, dtype, name, rel_rms=False):
+def assert_close(got, ref, dtype, name, rel_rms=False, scale=None):
+    """Max and mean |got - ref| within the bound of `dtype`, relative to RMS(ref) with
+    rel_rms.  `scale`: the RMS of a gradient of the same case that does not vanish
+    (dV); when the exact gradient is zero (every query sees a single key: P = 1
+    and dS = P (dP - Delta) = 0, so dQ = dK = 0), RMS(ref) is zero or float64
+    rounding noise, and the error is measured on that scale instead."""
     err = np.abs(np.asarray(got, dtype=np.float64) - ref)
     den = float(np.sqrt(np.mean(ref * ref))) if rel_rms else 1.0
+    if rel_rms and scale is not None and den < 1e-12 * scale:
+        den = scale
     mx, mean = err.max() / den, err.mean() / den
     if dtype == "f32":
         assert mx <= 1e-5, "%s: max err %.3e > 1e-5" % (name, mx)
@@ -85,7 +92,8 @@ def check_full(wl, res, backward=True):
     assert_lse(f64(res["lse"]), rl, wl.dtype)
     if backward:
         rg = oa.backward(q, k, v, ro, rl, do, wl.lens, wl.zigzag, wl.causal)
+        dv_rms = float(np.sqrt(np.mean(rg[2] * rg[2])))
         for name, g, r in zip(("dq", "dk", "dv"), res["grads"], rg):
-            assert_close(f64(g), r, wl.dtype, name, rel_rms=True)
+            assert_close(f64(g), r, wl.dtype, name, rel_rms=True, scale=dv_rms)
 
 

@@ -94,6 +94,19 @@ def test_d64_causal_bf16_gradients_many_tiles():
         assert excess.max() <= 1e-2 and excess.mean() <= 1e-3, (name, excess.max(), excess.mean())
 
 
+@pytest.mark.parametrize("d,causal,dtype", [(64, False, "f32"), (64, True, "bf16"), (128, False, "bf16"),
+                                             (128, True, "bf16")])
+def test_single_token_sequence(d, causal, dtype):
+    """The degenerate layout: one shard of one token (S = 1).  out = v and lse is the one score; the softmax
+    over a single key is constant, so dS = 0, the exact dQ and dK are zero and dV = dO.  dQ and dK are held to
+    the bound on the scale of dV, since their own RMS is zero."""
+    wl = Workload("one_token", B=2, H=3, d=d, lens=(1,), causal=causal, zigzag=False, dtype=dtype)
+    res = run_case(wl, seed=5)
+    check_full(wl, res)
+    q, k, v, do = (f64(x) for x in res["in"])
+    assert np.array_equal(f64(res["out"]), v), "out is not v"
+
+
 def test_backward_with_bf16_out():
     """The backward also accepts the forward output in bf16 (Delta then carries
     its rounding); on a non-causal case the gradients still meet the bound."""

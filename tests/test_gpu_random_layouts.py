@@ -102,5 +102,6 @@ def test_random_layout_ring_on_one_gpu(i, B, H, d, lens, causal, zigzag):
     assert_close(out, ro, "bf16", "out")
     assert_lse(lse, rl, "bf16")
     gq, gk, gv = oa.backward(Q, K, V, ro, rl, DO, lens, zigzag, causal)
+    dv_rms = float(np.sqrt(np.mean(gv * gv)))
     for name, got, ref in (("dq", dqs, gq), ("dk", dks, gk), ("dv", dvs, gv)):
-        assert_close(np.concatenate([f64(x) for x in got], axis=1), ref, "bf16", name, rel_rms=True)
+        assert_close(np.concatenate([f64(x) for x in got], axis=1), ref, "bf16", name, rel_rms=True, scale=dv_rms)
