@@ -288,6 +288,19 @@ def test_backward_matches_torch_autograd(causal):
         np.testing.assert_allclose(mine, t.grad.permute(0, 2, 1, 3).numpy(), atol=1e-11)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_single_key_closed_form(causal):
+    """One token (S = 1): P = 1 and Delta = dP, so dS = P (dP - Delta) = 0 -- dQ = dK = 0 and dV = dO (the
+    textbook backward with a constant softmax).  Catches a Delta or P that is not exactly the forward's."""
+    B, H, d = 2, 3, 16
+    q, k, v, do = (rnd((B, 1, H, d), s) for s in (61, 62, 63, 64))
+    out, lse = oa.forward(q, k, v, [1], causal=causal)
+    dq, dk, dv = oa.backward(q, k, v, out, lse, do, [1], causal=causal)
+    np.testing.assert_allclose(dv, do, rtol=1e-15)
+    scale = np.abs(do).max() * np.abs(v).max() * np.abs(k).max()
+    assert np.abs(dq).max() <= 1e-13 * scale and np.abs(dk).max() <= 1e-13 * scale
+
+
 def test_backward_invariants_under_zigzag():
     lens = [6, 2, 10, 4]
     S, d = sum(lens), 8
